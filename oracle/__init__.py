@@ -1,0 +1,22 @@
+"""CPU oracle for the block-scaled low-precision GEMM.  TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The product
+path (``fp4_gemm_gb300``) never imports it, and it never imports the product:
+the two share no code, tables or constants.  Inputs come from ``synth``.
+
+Contents (each function cites the passage it follows):
+
+* ``formats``  bit-field decoders and round-to-nearest-even encoders for FP8
+               E4M3 (fn) / E5M2, FP4 E2M1 and the E8M0 scale.
+* ``quantize`` the per-tile FP8 quantiser (scale = max_abs / format max) and the
+               MXFP4 quantiser (E8M0 per 32 elements along K, nibble packing).
+* ``gemm``     D = sum_k (s_A a_k)(s_B b_k) + C in FP64, with the per-element
+               error bound sum_k |s_A a_k s_B b_k| used by the tolerance.
+* ``fda``      the Hopper FP8 MMA bit model (aligned truncated sum, RZ-E8M13)
+               used only to interpret hardware results, never as the
+               correctness reference.
+
+Everything is plain numpy in FP64 (FP32 where the method fixes FP32), slow and
+written to be checked against the pages by eye.
+"""

@@ -1,0 +1,142 @@
+"""Quantisers of the block-scaled GEMM (CPU oracle; test infrastructure only).
+
+FP8 per-tile quantiser - "FP8 GEMM on CDNA4", §3.3 and §4.2:
+  the scale of a tile is its largest magnitude divided by the format's largest
+  value (448 for E4M3), every element is divided by the scale and stored as
+  FP8, and the GEMM multiplies the accumulated result by s_A * s_B (§4.4).
+  The tile is the granularity the page settles on (§3.3, §6); the workloads add
+  a 1 x 128 granularity for activations.
+
+MXFP4 quantiser - "Rubin FP4 GEMM deep dive", §4.2 steps 1-3 and §2.2:
+  per block of 32 elements along K, take the largest magnitude, divide by 6
+  (the E2M1 maximum), round that to the nearest power of two and store it as
+  an E8M0 code, divide the elements by the power of two, round to E2M1 and
+  pack two codes per byte, first element in the low nibble.
+
+Readings where the pages leave a step open (also listed in the design notes):
+  * the scale is s = max_abs / fmt_max computed in FP32 with round-to-nearest,
+    and the element is q = RNE_satfinite(x / s) with an IEEE FP32 division
+    (not a multiplication by 1/s);
+  * fmt_max is the format's own maximum: 448 for E4M3, 57344 for E5M2; any
+    other positive value may be passed (e.g. 448 for E5M2);
+  * an all-zero group (or one whose FP32 scale underflows to 0) gets s = 1.0;
+  * "nearest power of two" is nearest in linear distance on v = max_abs / 6
+    (FP32); a tie (v = 1.5 * 2^e) goes to the larger power; v = 0 gives
+    E8M0 code 127 (1.0); codes are clamped to [0, 254].
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import formats
+
+TILE = 128        # FP8 scale tile along both dimensions (and along K for 1x128)
+MX_BLOCK = 32     # MXFP4 block along K
+
+
+def _cdiv(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def fmt_max_default(fmt: str) -> float:
+    return formats.max_finite(fmt)
+
+
+def fp8_scale(amax: np.float32, fmt_max: float) -> np.float32:
+    """s = max_abs / fmt_max in FP32 (round to nearest); 1.0 if that is 0."""
+    s = np.float32(amax) / np.float32(fmt_max)
+    if s == 0:
+        s = np.float32(1.0)
+    return np.float32(s)
+
+
+def quantize_fp8(x: np.ndarray, fmt: str, gran: str, fmt_max: float | None = None):
+    """Quantise a row-major float32 matrix (rows x cols, cols = K) to FP8.
+
+    gran = "tile"  : one scale per 128 x 128 tile, scales[ceil(R/128)][ceil(C/128)]
+    gran = "row"   : one scale per 1 x 128 run of a row, stored K-tile major,
+                     scales[ceil(C/128)][R]
+    Ragged edge tiles cover what is left.  Returns (codes uint8 R x C,
+    scales float32).
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    R, C = x.shape
+    fm = fmt_max_default(fmt) if fmt_max is None else float(fmt_max)
+    codes = np.empty((R, C), dtype=np.uint8)
+    if gran == "tile":
+        scales = np.empty((_cdiv(R, TILE), _cdiv(C, TILE)), dtype=np.float32)
+        for ti in range(scales.shape[0]):
+            for tj in range(scales.shape[1]):
+                blk = x[ti * TILE:(ti + 1) * TILE, tj * TILE:(tj + 1) * TILE]
+                s = fp8_scale(np.max(np.abs(blk)), fm)
+                scales[ti, tj] = s
+                codes[ti * TILE:(ti + 1) * TILE, tj * TILE:(tj + 1) * TILE] = \
+                    formats.encode(blk / s, fmt)
+    elif gran == "row":
+        scales = np.empty((_cdiv(C, TILE), R), dtype=np.float32)
+        for tj in range(scales.shape[0]):
+            blk = x[:, tj * TILE:(tj + 1) * TILE]
+            amax = np.max(np.abs(blk), axis=1)
+            s = np.array([fp8_scale(a, fm) for a in amax], dtype=np.float32)
+            scales[tj, :] = s
+            codes[:, tj * TILE:(tj + 1) * TILE] = formats.encode(blk / s[:, None], fmt)
+    else:
+        raise ValueError(gran)
+    return codes, scales
+
+
+def e8m0_nearest_pow2(v: np.float32) -> int:
+    """E8M0 code of the power of two nearest to v (linear distance, ties up)."""
+    v = float(np.float32(v))
+    if v == 0.0:
+        return 127
+    f, x = math.frexp(v)            # v = f * 2^x, 0.5 <= f < 1, exact
+    lower = math.ldexp(1.0, x - 1)  # 2^floor(log2 v)
+    upper = 2.0 * lower
+    e = (x - 1) if (v - lower) < (upper - v) else x
+    return int(min(max(e + 127, 0), 254))
+
+
+def quantize_mxfp4(x: np.ndarray):
+    """Quantise a row-major float32 matrix (rows x K, K % 32 == 0) to MXFP4.
+
+    Returns (packed uint8 R x K/2, sf uint8 R x K/32) with the scale factors in
+    the canonical row-major layout.
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    R, K = x.shape
+    if K % MX_BLOCK:
+        raise ValueError("K must be a multiple of 32")
+    nb = K // MX_BLOCK
+    sf = np.empty((R, nb), dtype=np.uint8)
+    codes = np.empty((R, K), dtype=np.uint8)
+    blocks = x.reshape(R, nb, MX_BLOCK)
+    amax = np.max(np.abs(blocks), axis=2)
+    v = amax / np.float32(6.0)                     # FP32, round to nearest
+    for r in range(R):
+        for b in range(nb):
+            sf[r, b] = e8m0_nearest_pow2(v[r, b])
+    pow2 = np.ldexp(1.0, -(sf.astype(np.int64) - 127))    # 2^-E, exact in FP64
+    scaled = blocks.astype(np.float64) * pow2[:, :, None]  # exact
+    codes[:] = formats.encode(scaled.reshape(R, K), "e2m1")
+    return formats.pack_e2m1(codes), sf
+
+
+def sf_to_tcgen05_layout(sf: np.ndarray) -> np.ndarray:
+    """Rearrange row-major E8M0 scales [R][KB] into the storage order the
+    block-scaled tensor-core MMA reads them in (not from the pages; NVIDIA's
+    documented 128-row x 4-scale atom): atoms of 512 bytes, ordered by
+    (row block of 128, group of 4 K-blocks); inside an atom the byte of row r,
+    K-block c is at (r % 32) * 16 + ((r % 128) // 32) * 4 + (c % 4).
+    Padding bytes (rows beyond R, K-blocks beyond KB) hold code 127.
+    """
+    R, KB = sf.shape
+    rb, cb = _cdiv(R, 128), _cdiv(KB, 4)
+    out = np.full(rb * cb * 512, 127, dtype=np.uint8)
+    r = np.arange(R)[:, None]
+    c = np.arange(KB)[None, :]
+    off = ((r // 128) * cb + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + (c % 4)
+    out[off] = sf
+    return out
