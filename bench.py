@@ -1,0 +1,436 @@
+"""Benchmark of the block-scaled GEMM hot path on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Workloads (synthetic, seeded; see synth/):
+  ffn_up      FP8 FFN-up GEMM, M=8192 tokens, K=4096, N=14336.  One step =
+              quantise the FP32 activations to E4M3 with 1x128 scales, then the
+              promoted FP8 GEMM against pre-quantised E4M3 weights (128x128
+              scales), BF16 output.  Metric TFLOP/s (2MNK per step).   [default]
+  dgrad       FP8 dgrad GEMM, M=8192, K=14336, N=4096: E5M2 gradients (128x128
+              scales, quantised in the step) x E4M3 weights, FP32 output.
+  decode      MXFP4 decode, M=16 (or --m 1), K=8192, N=28672: quantise the BF16
+              activations to MXFP4, then the decode-shaped GEMM against
+              pre-quantised MXFP4 weights, BF16 out.  Metric GB/s of algorithmic
+              bytes (weights + scales + activations + output).
+  fp8_256, mxfp4_1024   the small parity configurations (latency-bound).
+
+One JSON line is printed by rank 0.  Timing: W warm-up steps, then K steps, each
+bracketed by CUDA events on the launching stream, with an L2 flush (a 256 MB
+write) before every timed step, outside the events.  The GEMM kernel is also
+timed alone per step (roofline).  `e2e` repeats the step through the same API
+with the activations copied from pinned host memory and the output copied back
+inside the timed region.  `cpu_baseline` times the CPU oracle on a bounded
+sample of the same workload.  Under torchrun every rank runs an independent
+replica ("replicas only": the path has no exchange step), value = sum over
+ranks, time = max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# nominal dense ratios to BF16 (2.25 PF): FP8 4.5 PF, FP4 13.5 PF
+RATIO = {"fp8": 2.0, "fp4": 6.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return FALLBACK, "fallback"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="ffn_up",
+                    choices=["ffn_up", "dgrad", "decode", "fp8_256", "mxfp4_1024"])
+    ap.add_argument("--m", type=int, default=None, help="override M (e.g. 1 for decode)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- workload
+class Workload:
+    """Inputs and one step of the hot path for a named workload."""
+
+    def __init__(self, name, m_override, dev):
+        import torch
+        import fp4_gemm_gb300 as bsg
+        self.bsg, self.torch, self.dev, self.name = bsg, torch, dev, name
+        idx, M, N, K = synth.WORKLOADS[name]
+        if m_override is not None:
+            M = m_override
+        self.M, self.N, self.K = M, N, K
+        A, B = synth.make(name, m=M)
+        self.fp4 = name in ("decode", "mxfp4_1024")
+        if name == "ffn_up":
+            self.fa, self.fb, self.ga, self.gb, self.out = "e4m3", "e4m3", "row", "tile", "bf16"
+        elif name == "dgrad":
+            self.fa, self.fb, self.ga, self.gb, self.out = "e5m2", "e4m3", "tile", "tile", "f32"
+        elif name == "fp8_256":
+            self.fa, self.fb, self.ga, self.gb, self.out = "e4m3", "e4m3", "tile", "tile", "f32"
+        elif name == "mxfp4_1024":
+            self.fa, self.fb, self.ga, self.gb, self.out = "e2m1", "e2m1", "mx", "mx", "f32"
+        else:
+            self.fa, self.fb, self.ga, self.gb, self.out = "e2m1", "e2m1", "mx", "mx", "bf16"
+        self.A_host = A
+        if name == "decode":
+            bits = synth.to_bf16_bits(A)
+            self.A_host_t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        else:
+            self.A_host_t = torch.from_numpy(A).pin_memory()
+        self.A = self.A_host_t.to(dev)
+        Bt = torch.from_numpy(B).to(dev)
+        # weights are quantised once, outside the step (static parameters)
+        if self.fp4:
+            self.qb, self.sb = bsg.bsg_quantize_mxfp4(Bt, "tcgen05")
+        else:
+            self.qb, self.sb = bsg.bsg_quantize_fp8(Bt, self.fb, self.gb)
+        del Bt
+        # step buffers (allocated once)
+        if self.fp4:
+            self.qa, self.sa = bsg.bsg_quantize_mxfp4(self.A, "tcgen05")
+        else:
+            self.qa, self.sa = bsg.bsg_quantize_fp8(self.A, self.fa, self.ga)
+        self.D = torch.empty((M, N), dtype=torch.bfloat16 if self.out == "bf16" else torch.float32,
+                             device=dev)
+        self.D_host = torch.empty_like(self.D, device="cpu").pin_memory()
+        self.ws = bsg.workspace_for(M, N, K, self.fa, self.fb, dev)
+        torch.cuda.synchronize()
+
+    def quantize(self):
+        b = self.bsg
+        if self.fp4:
+            b.bsg_quantize_mxfp4(self.A, "tcgen05", q=self.qa, sf=self.sa)
+        else:
+            b.bsg_quantize_fp8(self.A, self.fa, self.ga, q=self.qa, scales=self.sa)
+
+    def gemm(self):
+        self.bsg.bsg_gemm(self.qa, self.fa, self.sa, self.ga, self.qb, self.fb, self.sb, self.gb,
+                          out=self.out, D=self.D, workspace=self.ws, K=self.K)
+
+    def step(self):
+        self.quantize()
+        self.gemm()
+
+    launches_per_step = 2
+
+    # algorithmic quantities
+    def flops(self):
+        return 2.0 * self.M * self.N * self.K
+
+    def gemm_bytes(self):
+        """Bytes a GEMM must move at least once: operands, scales, output."""
+        M, N, K = self.M, self.N, self.K
+        if self.fp4:
+            a = M * K / 2 + M * K / 32
+            b = N * K / 2 + N * K / 32
+        else:
+            a = M * K + (M * -(-K // 128) * 4 if self.ga == "row" else 4 * -(-M // 128) * -(-K // 128))
+            b = N * K + 4 * -(-N // 128) * -(-K // 128)
+        d = M * N * (2 if self.out == "bf16" else 4)
+        return a + b + d
+
+    def step_bytes(self):
+        """Algorithmic bytes of a whole step (quantiser read + write, GEMM)."""
+        src = self.M * self.K * (2 if self.name == "decode" else 4)
+        return src + self.gemm_bytes()
+
+    def metric(self):
+        if self.name == "decode":
+            return "GB/s of algorithmic bytes (decode M<=16, % of HBM)", "GB/s"
+        return "GEMM TFLOP/s (% of GB300 dense FP8/FP4 peak)", "TFLOP/s"
+
+    def value_from_seconds(self, sec):
+        if self.name == "decode":
+            return self.step_bytes() / sec / 1e9
+        return self.flops() / sec / 1e12
+
+
+# ------------------------------------------------------------- clock sampler
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                c = [x.strip() for x in line.split(",")]
+                if len(c) < 9:
+                    continue
+                try:
+                    sm.append(float(c[1]))
+                    smax = float(c[2])
+                    power.append(float(c[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, c[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons)}
+        loaded = [s for s, p in zip(sm, power) if p > 0.5 * max(power)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- CPU baseline
+def cpu_baseline(name, m_override, target_s=15.0):
+    """The CPU oracle as it stands, on a bounded sample of the workload."""
+    import oracle.gemm as og
+    import oracle.quantize as oq
+    idx, M, N, K = synth.WORKLOADS[name]
+    if m_override is not None:
+        M = m_override
+    cores = os.cpu_count()
+    if name == "decode":
+        # a slice of the weight rows: quantise + GEMM, scaled to the metric (GB/s)
+        nrows = 4096
+        A, B = synth.make(name, m=M, n=nrows, k=K)
+        A = synth.bf16_bits_to_f32(synth.to_bf16_bits(A))
+        t0 = time.perf_counter()
+        pa, fa = oq.quantize_mxfp4(A)
+        pb, fb = oq.quantize_mxfp4(B)
+        og.gemm_mxfp4(pa, fa, pb, fb)
+        dt = time.perf_counter() - t0
+        nbytes = nrows * K / 2 + nrows * K / 32 + M * K * 2 + M * nrows * 2
+        return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                "sample": f"decode M={M}, {nrows} of {N} weight rows, K={K}: oracle quantise + GEMM, "
+                          f"{dt:.1f} s"}
+    fa, fb, ga, gb = {"ffn_up": ("e4m3", "e4m3", "row", "tile"),
+                      "dgrad": ("e5m2", "e4m3", "tile", "tile"),
+                      "fp8_256": ("e4m3", "e4m3", "tile", "tile"),
+                      "mxfp4_1024": ("e2m1", "e2m1", "mx", "mx")}[name]
+    rows = min(M, 128)
+    A, B = synth.make(name, m=rows)
+    t0 = time.perf_counter()
+    if fa == "e2m1":
+        pa, sfa = oq.quantize_mxfp4(A)
+        pb, sfb = oq.quantize_mxfp4(B)
+        og.gemm_mxfp4(pa, sfa, pb, sfb)
+    else:
+        qa, sa = oq.quantize_fp8(A, fa, ga)
+        qb, sb = oq.quantize_fp8(B, fb, gb)
+        og.gemm_fp8(qa, fa, sa, ga, qb, fb, sb, gb)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * N * K
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{name}: {rows} of {M} rows of A with all of B (N={N}, K={K}); oracle "
+                      f"quantise (both operands) + FP64 GEMM, {dt:.1f} s"}
+
+
+# -------------------------------------------------------------------- runs
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    cb = cpu_baseline(args.workload, args.m, target_s=10.0)
+    vals = []
+    for _ in range(args.warmup):
+        pass
+    for _ in range(max(1, min(args.steps, 3))):
+        vals.append(cpu_baseline(args.workload, args.m)["value"])
+    v = statistics.median(vals)
+    idx, M, N, K = synth.WORKLOADS[args.workload]
+    metric = ("GB/s of algorithmic bytes (decode M<=16, % of HBM)" if args.workload == "decode"
+              else "GEMM TFLOP/s (% of GB300 dense FP8/FP4 peak)")
+    line = {"impl": "reference", "metric": metric, "value": v, "unit": cb["unit"],
+            "n_gpus": world, "steps": len(vals), "warmup": args.warmup,
+            "higher_is_better": True, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "M": args.m or M, "N": N, "K": K},
+            "cpu_baseline": dict(cb, value=v),
+            "e2e": {"value": v, "unit": cb["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local, dist = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        if dist is not None:
+            dist.barrier()
+        return
+
+    import torch
+    import fp4_gemm_gb300 as bsg
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    bsg.load_library()
+    w = Workload(args.workload, args.m, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(args.warmup, 0)):
+        w.step()
+    torch.cuda.synchronize()
+    if bsg.bsg_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = Clocks(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(float(i))                       # L2 flush, outside the events
+        ev[i][0].record(stream)
+        w.quantize()
+        ev[i][1].record(stream)
+        w.gemm()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    if bsg.bsg_device_error() != 0:
+        raise RuntimeError("device error during the timed steps")
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    gemm_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    quant_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    ms = statistics.mean(step_ms)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        h2d = w.A_host_t.numel() * w.A_host_t.element_size()
+        d2h = w.D.numel() * w.D.element_size()
+        for _ in range(2):
+            w.A.copy_(w.A_host_t, non_blocking=True)
+            w.step()
+            w.D_host.copy_(w.D, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            w.A.copy_(w.A_host_t, non_blocking=True)
+            w.step()
+            w.D_host.copy_(w.D, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / K
+        if dist is not None:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * w.value_from_seconds(e_ms / 1e3), "unit": w.metric()[1],
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e_ms}
+
+    pk, pk_kind = peaks()
+    g_s = statistics.mean(gemm_ms) / 1e3
+    if w.name == "decode":
+        achieved = w.gemm_bytes() / g_s / 1e9
+        peak = pk["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": None,
+                "kernel": "gemm_mxfp4_decode_kernel",
+                "peak_source": f"{pk_kind} HBM copy bandwidth"}
+    else:
+        dt = "fp4" if w.fp4 else "fp8"
+        achieved = w.flops() / g_s / 1e12
+        peak = pk["bf16_tflops"] * RATIO[dt]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None,
+                "kernel": "gemm_mxfp4_kernel" if w.fp4 else "gemm_fp8_kernel",
+                "peak_source": f"{pk_kind} cuBLAS BF16 burst x {RATIO[dt]:g} (nominal dense "
+                               f"{dt.upper()}:BF16 ratio)"}
+    metric, unit = w.metric()
+    value = world * w.value_from_seconds(ms / 1e3)
+    line = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e2m1" if w.fp4 else (w.fa if w.fa == w.fb else f"{w.fa}x{w.fb}"),
+        "data": "synthetic (seeded; weights random-init and pre-quantised)",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+                   "a": f"{w.fa}/{w.ga}", "b": f"{w.fb}/{w.gb}", "out": w.out,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed (256 MB write) before every timed step"},
+        "quantize_ms": statistics.mean(quant_ms), "gemm_ms": statistics.mean(gemm_ms),
+        "wall_s": wall,
+        "roofline": roof,
+        "clocks": clk,
+        "gpu_launches": w.launches_per_step * K,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.m)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,223 @@
+"""Block-scaled FP8 / MXFP4 GEMM for GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over libbsg.so (include/bsg.h).  The functions carry the
+C entry points' names and only marshal arguments: torch allocates device
+memory and supplies the current stream; every step of the computation runs in
+the library's CUDA kernels.  There is no fallback: if libbsg.so has not been
+built, or no GPU is present, calls raise.
+
+    q, s   = bsg_quantize_fp8(x, "e4m3", "row")          # x: (rows, K) fp32/bf16 CUDA
+    qb, sf = bsg_quantize_mxfp4(w, layout="tcgen05")      # packed E2M1 + E8M0 scales
+    D      = bsg_gemm(qa, "e4m3", sa, "row", qw, "e4m3", sw, "tile", out="bf16")
+
+Operand B is K x N column-major, i.e. a (N, K) row-major tensor; D = A B.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libbsg.so")
+
+# enum values of include/bsg.h
+STATUS = {0: "BSG_OK", 1: "BSG_ERR_INVALID_ARG", 2: "BSG_ERR_UNSUPPORTED", 3: "BSG_ERR_ALIGNMENT",
+          4: "BSG_ERR_CUDA", 5: "BSG_ERR_TIMEOUT", 6: "BSG_ERR_WORKSPACE"}
+FORMAT = {"e4m3": 0, "e5m2": 1, "e2m1": 2}
+DTYPE = {"f32": 0, "bf16": 1}
+GRAN = {"tile": 0, "row": 1, "mx": 2}
+LAYOUT = {"rowmajor": 0, "tcgen05": 1}
+
+EXPORTS = ("bsg_quantize_fp8", "bsg_quantize_mxfp4", "bsg_gemm", "bsg_gemm_workspace_size",
+           "bsg_scale_bytes", "bsg_sf_to_tcgen05", "bsg_status_string", "bsg_device_error",
+           "bsg_num_sms")
+
+
+class BsgError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libbsg.so and declare the C signatures.  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is not built; run fp4_gemm_gb300.build.build() "
+                          "(there is no fallback implementation)")
+    lib = ctypes.CDLL(path)
+    c = ctypes
+    i64, vp, f32, i32, sz = c.c_int64, c.c_void_p, c.c_float, c.c_int, c.c_size_t
+    lib.bsg_quantize_fp8.argtypes = [vp, i32, i64, i64, i64, i32, i32, f32, vp, vp, vp]
+    lib.bsg_quantize_fp8.restype = i32
+    lib.bsg_quantize_mxfp4.argtypes = [vp, i32, i64, i64, i64, vp, vp, i32, vp]
+    lib.bsg_quantize_mxfp4.restype = i32
+    lib.bsg_gemm.argtypes = [i64, i64, i64, vp, i32, vp, i32, vp, i32, vp, i32, vp, vp, i32, vp, sz, vp]
+    lib.bsg_gemm.restype = i32
+    lib.bsg_gemm_workspace_size.argtypes = [i64, i64, i64, i32, i32]
+    lib.bsg_gemm_workspace_size.restype = sz
+    lib.bsg_scale_bytes.argtypes = [i64, i64, i32, i32]
+    lib.bsg_scale_bytes.restype = sz
+    lib.bsg_sf_to_tcgen05.argtypes = [vp, i64, i64, vp, vp]
+    lib.bsg_sf_to_tcgen05.restype = i32
+    lib.bsg_status_string.argtypes = [i32]
+    lib.bsg_status_string.restype = c.c_char_p
+    lib.bsg_device_error.argtypes = [vp]
+    lib.bsg_device_error.restype = i32
+    lib.bsg_num_sms.argtypes = []
+    lib.bsg_num_sms.restype = i32
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise BsgError(status, where)
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("bsg: every tensor must live on the GPU")
+
+
+# ----------------------------------------------------------------- sizes
+def bsg_scale_bytes(rows: int, cols: int, gran: str, layout: str = "rowmajor") -> int:
+    return int(load_library().bsg_scale_bytes(rows, cols, GRAN[gran], LAYOUT[layout]))
+
+
+def bsg_gemm_workspace_size(M: int, N: int, K: int, fa: str, fb: str) -> int:
+    return int(load_library().bsg_gemm_workspace_size(M, N, K, FORMAT[fa], FORMAT[fb]))
+
+
+def bsg_num_sms() -> int:
+    return int(load_library().bsg_num_sms())
+
+
+def bsg_status_string(status: int) -> str:
+    return load_library().bsg_status_string(status).decode()
+
+
+def bsg_device_error(stream=None) -> int:
+    """Synchronise and return (and clear) the device error status (0 = OK)."""
+    return int(load_library().bsg_device_error(_stream(stream)))
+
+
+# ------------------------------------------------------------ quantisers
+def bsg_quantize_fp8(x: torch.Tensor, fmt: str = "e4m3", gran: str = "tile",
+                     fmt_max: float = 0.0, q: torch.Tensor | None = None,
+                     scales: torch.Tensor | None = None, stream=None):
+    """x: (rows, K) FP32 or BF16 CUDA tensor (row stride = leading dimension).
+    Returns (codes uint8 (rows, K), scales float32): "tile" scales are
+    (ceil(rows/128), ceil(K/128)); "row" scales are (ceil(K/128), rows)."""
+    lib = load_library()
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D tensor with unit column stride")
+    rows, cols = x.shape
+    src = {torch.float32: 0, torch.bfloat16: 1}[x.dtype]
+    kt = -(-cols // 128)
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        shape = (-(-rows // 128), kt) if gran == "tile" else (kt, rows)
+        scales = torch.empty(shape, dtype=torch.float32, device=x.device)
+    _need_cuda(x, q, scales)
+    _check(lib.bsg_quantize_fp8(_ptr(x), src, rows, cols, x.stride(0), FORMAT[fmt], GRAN[gran],
+                                float(fmt_max), _ptr(q), _ptr(scales), _stream(stream)),
+           "bsg_quantize_fp8")
+    return q, scales
+
+
+def bsg_quantize_mxfp4(x: torch.Tensor, layout: str = "tcgen05", q: torch.Tensor | None = None,
+                       sf: torch.Tensor | None = None, stream=None):
+    """x: (rows, K) FP32 or BF16 CUDA tensor, K % 32 == 0.  Returns
+    (packed uint8 (rows, K/2), E8M0 scales uint8): "rowmajor" scales are
+    (rows, K/32); "tcgen05" scales are a flat buffer in the MMA's atom order."""
+    lib = load_library()
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D tensor with unit column stride")
+    rows, cols = x.shape
+    src = {torch.float32: 0, torch.bfloat16: 1}[x.dtype]
+    if q is None:
+        q = torch.empty((rows, cols // 2), dtype=torch.uint8, device=x.device)
+    if sf is None:
+        if layout == "rowmajor":
+            sf = torch.empty((rows, cols // 32), dtype=torch.uint8, device=x.device)
+        else:
+            n = lib.bsg_scale_bytes(rows, cols, GRAN["mx"], LAYOUT["tcgen05"])
+            sf = torch.empty((max(int(n), 1),), dtype=torch.uint8, device=x.device)
+    _need_cuda(x, q, sf)
+    _check(lib.bsg_quantize_mxfp4(_ptr(x), src, rows, cols, x.stride(0), _ptr(q), _ptr(sf),
+                                  LAYOUT[layout], _stream(stream)), "bsg_quantize_mxfp4")
+    return q, sf
+
+
+def bsg_sf_to_tcgen05(sf_rowmajor: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+    lib = load_library()
+    rows, kb = sf_rowmajor.shape
+    if out is None:
+        n = lib.bsg_scale_bytes(rows, kb * 32, GRAN["mx"], LAYOUT["tcgen05"])
+        out = torch.empty((int(n),), dtype=torch.uint8, device=sf_rowmajor.device)
+    _need_cuda(sf_rowmajor, out)
+    _check(lib.bsg_sf_to_tcgen05(_ptr(sf_rowmajor), rows, kb, _ptr(out), _stream(stream)),
+           "bsg_sf_to_tcgen05")
+    return out
+
+
+# ------------------------------------------------------------------ GEMM
+_workspaces: dict = {}
+
+
+def workspace_for(M: int, N: int, K: int, fa: str, fb: str, device) -> torch.Tensor | None:
+    """A zero-filled workspace of the size bsg_gemm needs, cached per device
+    (the library leaves it zero-filled after each call, so it is reused)."""
+    n = bsg_gemm_workspace_size(M, N, K, fa, fb)
+    if n == 0:
+        return None
+    dev = torch.device(device)
+    key = (dev.type, dev.index)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < n:
+        ws = torch.zeros((n,), dtype=torch.uint8, device=dev)
+        _workspaces[key] = ws
+    return ws
+
+
+def bsg_gemm(A: torch.Tensor, fa: str, sA: torch.Tensor, ga: str,
+             B: torch.Tensor, fb: str, sB: torch.Tensor, gb: str,
+             C: torch.Tensor | None = None, out: str = "f32", D: torch.Tensor | None = None,
+             workspace: torch.Tensor | None = None, K: int | None = None, stream=None):
+    """D = sum_k (s_A a_k)(s_B b_k) + C.  A: (M, K) codes (E2M1: (M, K/2)
+    packed); B: (N, K) codes (K x N column-major).  Returns D (M, N)."""
+    lib = load_library()
+    M = A.shape[0]
+    N = B.shape[0]
+    if K is None:
+        K = A.shape[1] * (2 if fa == "e2m1" else 1)
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.float32 if out == "f32" else torch.bfloat16,
+                        device=A.device)
+    if workspace is None:
+        workspace = workspace_for(M, N, K, fa, fb, A.device)
+    _need_cuda(A, sA, B, sB, C, D, workspace)
+    _check(lib.bsg_gemm(M, N, K, _ptr(A), FORMAT[fa], _ptr(sA), GRAN[ga], _ptr(B), FORMAT[fb],
+                        _ptr(sB), GRAN[gb], _ptr(C), _ptr(D), DTYPE[out], _ptr(workspace),
+                        0 if workspace is None else workspace.numel(), _stream(stream)),
+           "bsg_gemm")
+    return D

@@ -1,0 +1,261 @@
+// The C ABI of libbsg.so (declared in include/bsg.h): host-side validation,
+// TMA descriptor encoding and dispatch to the kernels.  Nothing here
+// allocates device memory.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "bsg.h"
+#include "kernels.h"
+
+namespace {
+
+using bsg::Fp8GemmArgs;
+using bsg::Mxfp4GemmArgs;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D byte matrix `rows` x `inner_bytes` with a row pitch, loaded in boxes of
+// box_rows x 128 bytes with 128-byte swizzling; out-of-range reads are 0.
+bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
+                     uint64_t pitch, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner_bytes, rows};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms_current() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bsg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BSG_OK : BSG_ERR_CUDA; }
+
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
+
+bool is_fp8(bsg_format f) { return f == BSG_E4M3 || f == BSG_E5M2; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Rows of the activation operand up to which E2M1 GEMMs take the
+// decode-shaped path (weights streamed once, swap-AB, split-K).
+constexpr int64_t kDecodeMaxM = 32;
+
+}  // namespace
+
+extern "C" {
+
+const char* bsg_status_string(bsg_status s) {
+  switch (s) {
+    case BSG_OK: return "BSG_OK";
+    case BSG_ERR_INVALID_ARG: return "BSG_ERR_INVALID_ARG";
+    case BSG_ERR_UNSUPPORTED: return "BSG_ERR_UNSUPPORTED";
+    case BSG_ERR_ALIGNMENT: return "BSG_ERR_ALIGNMENT";
+    case BSG_ERR_CUDA: return "BSG_ERR_CUDA";
+    case BSG_ERR_TIMEOUT: return "BSG_ERR_TIMEOUT";
+    case BSG_ERR_WORKSPACE: return "BSG_ERR_WORKSPACE";
+  }
+  return "BSG_ERR_UNKNOWN";
+}
+
+int bsg_num_sms(void) { return num_sms_current(); }
+
+size_t bsg_scale_bytes(int64_t rows, int64_t cols, bsg_scale_gran gran, bsg_sf_layout layout) {
+  if (rows <= 0 || cols <= 0) return 0;
+  switch (gran) {
+    case BSG_SCALE_TILE128x128:
+      return static_cast<size_t>(cdiv(rows, 128) * cdiv(cols, 128)) * sizeof(float);
+    case BSG_SCALE_ROW1x128:
+      return static_cast<size_t>(rows * cdiv(cols, 128)) * sizeof(float);
+    case BSG_SCALE_BLOCK1x32_E8M0:
+      if (cols % 32) return 0;
+      if (layout == BSG_SF_TCGEN05)
+        return static_cast<size_t>(cdiv(rows, 128) * cdiv(cols / 32, 4) * 512);
+      return static_cast<size_t>(rows * (cols / 32));
+  }
+  return 0;
+}
+
+bsg_status bsg_quantize_fp8(const void* x, bsg_dtype src, int64_t rows, int64_t cols, int64_t ld,
+                            bsg_format fmt, bsg_scale_gran gran, float fmt_max, uint8_t* q,
+                            float* scales, void* stream) {
+  if (x == nullptr || q == nullptr || scales == nullptr) return BSG_ERR_INVALID_ARG;
+  if (rows <= 0 || cols <= 0 || ld < cols || rows > kMaxDim || cols > kMaxDim)
+    return BSG_ERR_INVALID_ARG;
+  if (src != BSG_F32 && src != BSG_BF16) return BSG_ERR_INVALID_ARG;
+  if (!(fmt_max >= 0.0f) || !std::isfinite(fmt_max)) return BSG_ERR_INVALID_ARG;
+  if (!is_fp8(fmt)) return BSG_ERR_UNSUPPORTED;
+  if (gran != BSG_SCALE_TILE128x128 && gran != BSG_SCALE_ROW1x128) return BSG_ERR_UNSUPPORTED;
+  if (!aligned(x, src == BSG_F32 ? 4 : 2) || !aligned(scales, 4)) return BSG_ERR_ALIGNMENT;
+  if (gran == BSG_SCALE_TILE128x128 && cdiv(rows, 128) > 65535) return BSG_ERR_INVALID_ARG;
+  const float fm = fmt_max == 0.0f ? (fmt == BSG_E4M3 ? 448.0f : 57344.0f) : fmt_max;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int f = fmt == BSG_E4M3 ? 0 : 1;
+  if (gran == BSG_SCALE_TILE128x128)
+    return from_cuda(bsg::launch_quantize_fp8_tile(x, src == BSG_BF16, rows, cols, ld, f, fm, q,
+                                                   scales, s));
+  return from_cuda(
+      bsg::launch_quantize_fp8_row(x, src == BSG_BF16, rows, cols, ld, f, fm, q, scales, s));
+}
+
+bsg_status bsg_quantize_mxfp4(const void* x, bsg_dtype src, int64_t rows, int64_t cols,
+                              int64_t ld, uint8_t* q_packed, uint8_t* sf, bsg_sf_layout layout,
+                              void* stream) {
+  if (x == nullptr || q_packed == nullptr || sf == nullptr) return BSG_ERR_INVALID_ARG;
+  if (rows <= 0 || cols <= 0 || ld < cols || rows > kMaxDim || cols > kMaxDim || cols % 32)
+    return BSG_ERR_INVALID_ARG;
+  if (src != BSG_F32 && src != BSG_BF16) return BSG_ERR_INVALID_ARG;
+  if (layout != BSG_SF_ROWMAJOR && layout != BSG_SF_TCGEN05) return BSG_ERR_INVALID_ARG;
+  if (!aligned(x, src == BSG_F32 ? 4 : 2) || !aligned(q_packed, 4)) return BSG_ERR_ALIGNMENT;
+  return from_cuda(bsg::launch_quantize_mxfp4(x, src == BSG_BF16, rows, cols, ld, q_packed, sf,
+                                              layout == BSG_SF_TCGEN05,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+bsg_status bsg_sf_to_tcgen05(const uint8_t* sf_rowmajor, int64_t rows, int64_t kblocks,
+                             uint8_t* sf_tc, void* stream) {
+  if (sf_rowmajor == nullptr || sf_tc == nullptr || rows <= 0 || kblocks <= 0 ||
+      rows > kMaxDim || kblocks > kMaxDim)
+    return BSG_ERR_INVALID_ARG;
+  return from_cuda(
+      bsg::launch_sf_to_tcgen05(sf_rowmajor, rows, kblocks, sf_tc, static_cast<cudaStream_t>(stream)));
+}
+
+size_t bsg_gemm_workspace_size(int64_t M, int64_t N, int64_t K, bsg_format fa, bsg_format fb) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  if (fa == BSG_E2M1 && fb == BSG_E2M1 && M <= kDecodeMaxM) {
+    const int sms = num_sms_current();
+    return bsg::gemm_mxfp4_decode_workspace(static_cast<int>(M), static_cast<int>(N),
+                                            static_cast<int>(K), sms > 0 ? sms : 1);
+  }
+  return 0;
+}
+
+bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format fa, const void* sA,
+                    bsg_scale_gran ga, const void* B, bsg_format fb, const void* sB,
+                    bsg_scale_gran gb, const float* C, void* D, bsg_dtype out, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  if (A == nullptr || B == nullptr || sA == nullptr || sB == nullptr || D == nullptr)
+    return BSG_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return BSG_ERR_INVALID_ARG;
+  if (out != BSG_F32 && out != BSG_BF16) return BSG_ERR_INVALID_ARG;
+  if (fa < BSG_E4M3 || fa > BSG_E2M1 || fb < BSG_E4M3 || fb > BSG_E2M1) return BSG_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16)) return BSG_ERR_ALIGNMENT;
+  if (!aligned(D, out == BSG_F32 ? 4 : 2) || (C != nullptr && !aligned(C, 4)))
+    return BSG_ERR_ALIGNMENT;
+  const bool fp8 = is_fp8(fa) && is_fp8(fb);
+  const bool fp4 = fa == BSG_E2M1 && fb == BSG_E2M1;
+  if (!fp8 && !fp4) return BSG_ERR_UNSUPPORTED;
+  if (fp8) {
+    if (ga != BSG_SCALE_TILE128x128 && ga != BSG_SCALE_ROW1x128) return BSG_ERR_UNSUPPORTED;
+    if (gb != BSG_SCALE_TILE128x128 && gb != BSG_SCALE_ROW1x128) return BSG_ERR_UNSUPPORTED;
+    if (K % 16) return BSG_ERR_INVALID_ARG;
+    if (!aligned(sA, 4) || !aligned(sB, 4)) return BSG_ERR_ALIGNMENT;
+  } else {
+    if (ga != BSG_SCALE_BLOCK1x32_E8M0 || gb != BSG_SCALE_BLOCK1x32_E8M0) return BSG_ERR_UNSUPPORTED;
+    if (K % 32) return BSG_ERR_INVALID_ARG;
+    if (!aligned(sA, 16) || !aligned(sB, 16)) return BSG_ERR_ALIGNMENT;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int sms = num_sms_current();
+  if (sms <= 0) return BSG_ERR_CUDA;
+
+  if (fp8) {
+    Fp8GemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.afmt = fa == BSG_E4M3 ? 0 : 1;
+    a.bfmt = fb == BSG_E4M3 ? 0 : 1;
+    a.sA = static_cast<const float*>(sA);
+    a.a_row = ga == BSG_SCALE_ROW1x128;
+    a.sB = static_cast<const float*>(sB);
+    a.b_row = gb == BSG_SCALE_ROW1x128;
+    a.C = C;
+    a.D = D;
+    a.out_bf16 = out == BSG_BF16;
+    if (!make_kmajor_map(&a.tmA, A, K, M, K, 128) || !make_kmajor_map(&a.tmB, B, K, N, K, 256))
+      return BSG_ERR_CUDA;
+    return from_cuda(bsg::launch_gemm_fp8(a, sms, s));
+  }
+  {
+    Mxfp4GemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.sfA = static_cast<const uint8_t*>(sA);
+    a.sfB = static_cast<const uint8_t*>(sB);
+    a.C = C;
+    a.D = D;
+    a.out_bf16 = out == BSG_BF16;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    if (M <= kDecodeMaxM) {
+      const size_t need = bsg::gemm_mxfp4_decode_workspace(a.M, a.N, a.K, sms);
+      if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)))
+        return BSG_ERR_WORKSPACE;
+      // swap-AB: the weights (B, N rows) are the MMA's 128-row operand
+      const uint32_t xrows = M <= 16 ? 16 : 32;
+      if (!make_kmajor_map(&a.tmA, A, K / 2, M, K / 2, xrows) ||
+          !make_kmajor_map(&a.tmB, B, K / 2, N, K / 2, 128))
+        return BSG_ERR_CUDA;
+      return from_cuda(bsg::launch_gemm_mxfp4_decode(a, sms, s));
+    }
+    if (!make_kmajor_map(&a.tmA, A, K / 2, M, K / 2, 128) ||
+        !make_kmajor_map(&a.tmB, B, K / 2, N, K / 2, 128))
+      return BSG_ERR_CUDA;
+    return from_cuda(bsg::launch_gemm_mxfp4(a, sms, s));
+  }
+}
+
+bsg_status bsg_device_error(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BSG_ERR_CUDA;
+  uint32_t w0 = 0, w1 = 0, w2 = 0;
+  if (bsg::quantize_error_read_and_clear(s, &w0) != cudaSuccess ||
+      bsg::gemm_fp8_error_read_and_clear(s, &w1) != cudaSuccess ||
+      bsg::gemm_mxfp4_error_read_and_clear(s, &w2) != cudaSuccess)
+    return BSG_ERR_CUDA;
+  const uint32_t w = w0 | w1 | w2;
+  if (w & 1u) return BSG_ERR_TIMEOUT;
+  if (w & 2u) return BSG_ERR_WORKSPACE;
+  return BSG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,371 @@
+// FP8 block-scaled GEMM with per-K-tile promotion, for sm_103a.
+//
+//   D[i][j] = sum_t (s_A(i,t) * s_B(j,t)) * P_t[i][j] + C[i][j]
+//   P_t     = sum_{k in K tile t} a[i][k] * b[j][k]      (128-wide K tiles)
+//
+// The per-tile FP32 scales of "FP8 GEMM on CDNA4" (section 3.3, multiplied
+// back after accumulation in section 4.4) are not powers of two, so they can
+// not ride inside the tensor core.  Each 128-wide K tile's partial product
+// P_t is formed by four tcgen05.mma (K = 32 each) into a tensor-memory
+// buffer, then drained by CUDA-core warps that compute
+//     acc = fmaf(s_A * s_B, P_t, acc)
+// in an FP32 register accumulator.  This is the promotion that
+// "FP8 MMA internals on Hopper" motivates (a chained tensor-core accumulator
+// sets the alignment exponent and drops small terms); on GB300 the partial
+// lives in tensor memory, double-buffered, so the MMA of tile t+1 overlaps
+// the drain of tile t.
+//
+// Warp roles (320 threads, one CTA per SM, persistent over output tiles):
+//   warps 0-7  promotion + epilogue.  Warp w reads TMEM lanes 32*(w%4)..+31
+//              (its rows) and column half w/4 of the 256-wide tile.
+//   warp 8     producer: TMA loads of A (128 x 128 B) and B (256 x 128 B)
+//              into a 4-stage ring; cp.async of the K tile's scales into an
+//              8-slot scale ring.
+//   warp 9     tensor-memory allocator and MMA issuer (one elected lane).
+// Every wait is bounded; a wait that runs out sets the error word, raises a
+// CTA-wide abort flag and all roles unwind to the final barrier.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bsg {
+namespace {
+
+__device__ uint32_t g_fp8_error = 0;
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;            // one scale tile along K = one promotion unit
+constexpr int kStages = 4;
+constexpr int kScaleSlots = 8;
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kTmemCols = 512;     // two 256-column FP32 partial buffers
+constexpr int kGroupM = 8;         // tile raster: groups of 8 M tiles
+
+struct __align__(1024) Smem {
+  uint8_t a[kStages][BM * BK];
+  uint8_t b[kStages][BN * BK];
+  float sa[kScaleSlots][BM];
+  float sb[kScaleSlots][BN];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t sfull[kScaleSlots];
+  uint64_t sempty[kScaleSlots];
+  uint64_t final_bar;
+  uint32_t tmem_base;
+  volatile uint32_t abort_flag;
+};
+
+struct TileCoord {
+  int m, n;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(int t, int num_m, int num_n) {
+  const int group_size = kGroupM * num_n;
+  const int group = t / group_size;
+  const int first_m = group * kGroupM;
+  const int gsz = min(num_m - first_m, kGroupM);
+  const int local = t % group_size;
+  return {first_m + local % gsz, local / gsz};
+}
+
+__device__ __forceinline__ void raise_abort(Smem& sm) {
+  atomicOr(&g_fp8_error, kErrTimeout);
+  sm.abort_flag = 1u;
+}
+
+template <bool kARow, bool kBRow, bool kBF16Out>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const float* __restrict__ sA, const float* __restrict__ sB,
+                    const float* __restrict__ Cin, void* __restrict__ Dout, int M, int N, int K,
+                    uint32_t idesc, bool vec_out) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~static_cast<uintptr_t>(1023));
+  const int warp = static_cast<int>(warp_id());
+  const int lane = static_cast<int>(lane_id());
+  const int num_m = (M + BM - 1) / BM;
+  const int num_n = (N + BN - 1) / BN;
+  const int tiles = num_m * num_n;
+  const int KT = (K + BK - 1) / BK;
+  const int num_nb = (N + 127) / 128;   // 128-wide scale blocks of B
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&sm.full[s]), 1);
+      mbar_init(smem_u32(&sm.empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sm.tfull[b]), 1);
+      mbar_init(smem_u32(&sm.tempty[b]), 8);
+    }
+    for (int s = 0; s < kScaleSlots; ++s) {
+      mbar_init(smem_u32(&sm.sfull[s]), 32);
+      mbar_init(smem_u32(&sm.sempty[s]), 8);
+    }
+    mbar_init(smem_u32(&sm.final_bar), 1);
+    sm.abort_flag = 0u;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      const TileCoord tc = tile_coord(t, num_m, num_n);
+      for (int kt = 0; kt < KT; ++kt, ++it) {
+        if (sm.abort_flag) { ok = false; break; }
+        const int s = static_cast<int>(it % kStages);
+        const uint32_t ph = (it / kStages) & 1u;
+        const int ss = static_cast<int>(it % kScaleSlots);
+        const uint32_t phs = (it / kScaleSlots) & 1u;
+        int good = 1;
+        if (lane == 0) {
+          good = mbar_wait(smem_u32(&sm.empty[s]), ph ^ 1u) &&
+                 mbar_wait(smem_u32(&sm.sempty[ss]), phs ^ 1u);
+          if (good) {
+            const uint32_t fb = smem_u32(&sm.full[s]);
+            mbar_arrive_expect_tx(fb, (BM + BN) * BK);
+            tma_load_2d(smem_u32(sm.a[s]), &tmA, fb, kt * BK, tc.m * BM);
+            tma_load_2d(smem_u32(sm.b[s]), &tmB, fb, kt * BK, tc.n * BN);
+          } else {
+            raise_abort(sm);
+          }
+        }
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) { ok = false; break; }
+        // scales of this K tile -> scale slot ss
+        if (kARow) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = tc.m * BM + 4 * lane + j;
+            if (r < M) cp_async_4(smem_u32(&sm.sa[ss][4 * lane + j]), sA + static_cast<int64_t>(kt) * M + r);
+          }
+        } else if (lane == 0) {
+          cp_async_4(smem_u32(&sm.sa[ss][0]), sA + static_cast<int64_t>(tc.m) * KT + kt);
+        }
+        if (kBRow) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int c = tc.n * BN + 8 * lane + j;
+            if (c < N) cp_async_4(smem_u32(&sm.sb[ss][8 * lane + j]), sB + static_cast<int64_t>(kt) * N + c);
+          }
+        } else if (lane < BN / 128) {
+          const int nb = tc.n * (BN / 128) + lane;
+          if (nb < num_nb)
+            cp_async_4(smem_u32(&sm.sb[ss][128 * lane]), sB + static_cast<int64_t>(nb) * KT + kt);
+        }
+        cp_async_mbar_arrive_noinc(smem_u32(&sm.sfull[ss]));
+      }
+    }
+    cp_async_wait_all();
+    if (lane == 0) drain_fills(sm.full, kStages, it);
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          if (sm.abort_flag) { ok = false; break; }
+          const uint32_t b = it & 1u;
+          const uint32_t tph = (it >> 1) & 1u;
+          const int s = static_cast<int>(it % kStages);
+          const uint32_t ph = (it / kStages) & 1u;
+          if (!mbar_wait(smem_u32(&sm.tempty[b]), tph ^ 1u) ||
+              !mbar_wait(smem_u32(&sm.full[s]), ph)) {
+            raise_abort(sm);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sm.a[s]));
+          const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sm.b[s]));
+          const uint32_t d = tmem + b * BN;
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk)
+            mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+          tc_commit(smem_u32(&sm.empty[s]));
+          tc_commit(smem_u32(&sm.tfull[b]));
+        }
+      }
+      // every MMA this thread issued has completed once final_bar flips
+      tc_commit(smem_u32(&sm.final_bar));
+      if (!mbar_wait(smem_u32(&sm.final_bar), 0)) raise_abort(sm);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------- promotion + epilogue
+    const int q = warp & 3;          // TMEM lane quarter = rows 32q..32q+31
+    const int g = warp >> 2;         // column half of the 256-wide tile
+    const int row = q * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + g * 128;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      const TileCoord tc = tile_coord(t, num_m, num_n);
+      float acc[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      for (int kt = 0; kt < KT; ++kt, ++it) {
+        const uint32_t b = it & 1u;
+        const uint32_t tph = (it >> 1) & 1u;
+        const int ss = static_cast<int>(it % kScaleSlots);
+        const uint32_t phs = (it / kScaleSlots) & 1u;
+        if (sm.abort_flag || !mbar_wait(smem_u32(&sm.sfull[ss]), phs) ||
+            !mbar_wait(smem_u32(&sm.tfull[b]), tph)) {
+          if (!sm.abort_flag) raise_abort(sm);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float sa = kARow ? sm.sa[ss][row] : sm.sa[ss][0];
+        const float sc = kBRow ? sa : sa * sm.sb[ss][g * 128];
+        const uint32_t taddr = lane_base + b * BN;
+        uint32_t r0[16], r1[16];
+        tmem_ld_16(taddr, r0);
+        tc_wait_ld_16(r0);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t (&cur)[16] = (c & 1) ? r1 : r0;
+          uint32_t (&nxt)[16] = (c & 1) ? r0 : r1;
+          if (c + 1 < 8) tmem_ld_16(taddr + (c + 1) * 16, nxt);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float scj = kBRow ? sc * sm.sb[ss][g * 128 + c * 16 + j] : sc;
+            acc[c * 16 + j] = fmaf(scj, __uint_as_float(cur[j]), acc[c * 16 + j]);
+          }
+          if (c + 1 < 8) tc_wait_ld_16(nxt);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&sm.tempty[b]));
+          mbar_arrive(smem_u32(&sm.sempty[ss]));
+        }
+      }
+      if (!ok) break;
+      // ---- epilogue: rows of this thread, 128 columns of its half
+      const int64_t grow = static_cast<int64_t>(tc.m) * BM + row;
+      const int gcol0 = tc.n * BN + g * 128;
+      if (grow < M) {
+        if (kBF16Out) {
+          __nv_bfloat16* D = static_cast<__nv_bfloat16*>(Dout) + grow * N;
+#pragma unroll
+          for (int c = 0; c < 128; c += 8) {
+            const int col = gcol0 + c;
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = acc[c + j];
+            if (Cin != nullptr) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                if (col + j < N) v[j] += __ldg(Cin + grow * N + col + j);
+            }
+            if (vec_out && col + 7 < N) {
+              uint4 u;
+              u.x = pack_bf16x2(v[0], v[1]);
+              u.y = pack_bf16x2(v[2], v[3]);
+              u.z = pack_bf16x2(v[4], v[5]);
+              u.w = pack_bf16x2(v[6], v[7]);
+              *reinterpret_cast<uint4*>(D + col) = u;
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                if (col + j < N) D[col + j] = __float2bfloat16_rn(v[j]);
+            }
+          }
+        } else {
+          float* D = static_cast<float*>(Dout) + grow * N;
+#pragma unroll
+          for (int c = 0; c < 128; c += 4) {
+            const int col = gcol0 + c;
+            float v[4] = {acc[c], acc[c + 1], acc[c + 2], acc[c + 3]};
+            if (Cin != nullptr) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (col + j < N) v[j] += __ldg(Cin + grow * N + col + j);
+            }
+            if (vec_out && col + 3 < N) {
+              *reinterpret_cast<float4*>(D + col) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (col + j < N) D[col + j] = v[j];
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <bool kARow, bool kBRow, bool kBF16Out>
+cudaError_t launch_variant(const Fp8GemmArgs& a, int num_sms, cudaStream_t s) {
+  auto kern = gemm_fp8_kernel<kARow, kBRow, kBF16Out>;
+  const size_t smem = sizeof(Smem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  const uint32_t idesc = idesc_f8f6f4(static_cast<uint32_t>(a.afmt), static_cast<uint32_t>(a.bfmt), BM, BN);
+  const bool vec_out = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) &&
+                       (a.out_bf16 ? (a.N % 8 == 0) : (a.N % 4 == 0));
+  kern<<<grid, kThreads, smem, s>>>(a.tmA, a.tmB, a.sA, a.sB, a.C, a.D, a.M, a.N, a.K, idesc,
+                                    vec_out);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t gemm_fp8_error_read_and_clear(cudaStream_t s, uint32_t* out) {
+  uint32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_fp8_error, sizeof(uint32_t), 0,
+                                            cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyToSymbolAsync(g_fp8_error, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(s);
+}
+
+cudaError_t launch_gemm_fp8(const Fp8GemmArgs& a, int num_sms, cudaStream_t s) {
+  const int key = (a.a_row ? 4 : 0) | (a.b_row ? 2 : 0) | (a.out_bf16 ? 1 : 0);
+  switch (key) {
+    case 0: return launch_variant<false, false, false>(a, num_sms, s);
+    case 1: return launch_variant<false, false, true>(a, num_sms, s);
+    case 2: return launch_variant<false, true, false>(a, num_sms, s);
+    case 3: return launch_variant<false, true, true>(a, num_sms, s);
+    case 4: return launch_variant<true, false, false>(a, num_sms, s);
+    case 5: return launch_variant<true, false, true>(a, num_sms, s);
+    case 6: return launch_variant<true, true, false>(a, num_sms, s);
+    default: return launch_variant<true, true, true>(a, num_sms, s);
+  }
+}
+
+}  // namespace bsg

@@ -1,0 +1,65 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace bsg {
+
+// Each kernel translation unit owns one device error word.  read_and_clear
+// copies it to the host (synchronously on `s`) and zeroes it.
+cudaError_t quantize_error_read_and_clear(cudaStream_t s, uint32_t* out);
+cudaError_t gemm_fp8_error_read_and_clear(cudaStream_t s, uint32_t* out);
+cudaError_t gemm_mxfp4_error_read_and_clear(cudaStream_t s, uint32_t* out);
+
+// ------------------------------------------------------------- quantisers
+// src_bf16: source is BF16 (else FP32).  fmt: 0 E4M3, 1 E5M2.
+cudaError_t launch_quantize_fp8_tile(const void* x, bool src_bf16, int64_t rows, int64_t cols,
+                                     int64_t ld, int fmt, float fmt_max, uint8_t* q,
+                                     float* scales, cudaStream_t s);
+cudaError_t launch_quantize_fp8_row(const void* x, bool src_bf16, int64_t rows, int64_t cols,
+                                    int64_t ld, int fmt, float fmt_max, uint8_t* q, float* scales,
+                                    cudaStream_t s);
+// tc_layout: write scales in the tcgen05 atom layout (with padding) instead
+// of row-major.
+cudaError_t launch_quantize_mxfp4(const void* x, bool src_bf16, int64_t rows, int64_t cols,
+                                  int64_t ld, uint8_t* q, uint8_t* sf, bool tc_layout,
+                                  cudaStream_t s);
+cudaError_t launch_sf_to_tcgen05(const uint8_t* sf, int64_t rows, int64_t kblocks, uint8_t* out,
+                                 cudaStream_t s);
+
+// ----------------------------------------------------------------- GEMMs
+struct Fp8GemmArgs {
+  int M, N, K;
+  int afmt, bfmt;            // 0 E4M3, 1 E5M2
+  const float* sA;           // scales of A
+  bool a_row;                // A scales per 1x128 ([KT][M]) instead of 128x128 ([MT][KT])
+  const float* sB;
+  bool b_row;
+  const float* C;            // optional FP32 addend
+  void* D;
+  bool out_bf16;
+  CUtensorMap tmA, tmB;      // K-major operand maps (box 128 B x rows)
+};
+cudaError_t launch_gemm_fp8(const Fp8GemmArgs& a, int num_sms, cudaStream_t s);
+
+struct Mxfp4GemmArgs {
+  int M, N, K;
+  const uint8_t* sfA;        // tcgen05 layout
+  const uint8_t* sfB;
+  const float* C;
+  void* D;
+  bool out_bf16;
+  CUtensorMap tmA, tmB;      // packed operands (box 128 B x rows)
+  void* workspace;           // split-K partials + tile counters (decode path)
+  size_t workspace_bytes;
+};
+cudaError_t launch_gemm_mxfp4(const Mxfp4GemmArgs& a, int num_sms, cudaStream_t s);
+// Decode-shaped (small M) MXFP4 GEMM: weights B stream once; A has M <= 32 rows.
+size_t gemm_mxfp4_decode_workspace(int M, int N, int K, int num_sms);
+cudaError_t launch_gemm_mxfp4_decode(const Mxfp4GemmArgs& a, int num_sms, cudaStream_t s);
+
+}  // namespace bsg

@@ -1,0 +1,354 @@
+// Quantisers: FP32/BF16 -> FP8 (E4M3/E5M2) with FP32 per-tile scales, and
+// FP32/BF16 -> MXFP4 (E2M1 + E8M0 per 32 along K).
+//
+// FP8 ("FP8 GEMM on CDNA4", sections 3.3 and 4.2): each scale group's largest
+// magnitude comes from a warp-shuffle max reduction; s = max_abs / fmt_max in
+// FP32; every element is divided by s (IEEE division) and converted with the
+// hardware's round-to-nearest-even, saturating cvt.
+//
+// MXFP4 ("Rubin FP4 GEMM deep dive", section 4.2 steps 1-3): per 32-element
+// block v = max_abs / 6 in FP32; the E8M0 scale is the power of two nearest to
+// v (linear distance, ties to the larger), read off v's exponent field and its
+// first mantissa bit; elements are multiplied by the exact inverse power of
+// two and converted with cvt.rn.satfinite.e2m1x2; two codes per byte, the
+// first element in the low nibble.
+//
+// All kernels are single-pass and HBM-bound: each element is read once and
+// its code written once.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bsg {
+namespace {
+
+__device__ uint32_t g_quant_error = 0;
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Load 4 consecutive source elements starting at (row, col) as FP32; columns
+// at or beyond `cols` read as 0.
+template <bool kBF16>
+__device__ __forceinline__ void load4(const void* x, int64_t row, int64_t col, int64_t cols,
+                                      int64_t ld, bool vec_ok, float (&v)[4]) {
+  if (kBF16) {
+    const uint16_t* p = static_cast<const uint16_t*>(x) + row * ld + col;
+    if (vec_ok && col + 3 < cols) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+      v[0] = __uint_as_float(u.x << 16);
+      v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+      v[2] = __uint_as_float(u.y << 16);
+      v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = (col + j < cols) ? bf16_to_f32(p[j]) : 0.0f;
+    }
+  } else {
+    const float* p = static_cast<const float*>(x) + row * ld + col;
+    if (vec_ok && col + 3 < cols) {
+      const float4 u = __ldg(reinterpret_cast<const float4*>(p));
+      v[0] = u.x;
+      v[1] = u.y;
+      v[2] = u.z;
+      v[3] = u.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = (col + j < cols) ? p[j] : 0.0f;
+    }
+  }
+}
+
+// Four FP32 values -> four FP8 codes, first value in the lowest byte.
+__device__ __forceinline__ uint32_t cvt4_fp8(int fmt, float a, float b, float c, float d) {
+  uint16_t lo, hi;
+  if (fmt == 0) {
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  } else {
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  }
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+__device__ __forceinline__ float fp8_scale(float amax, float fmt_max) {
+  float s = __fdiv_rn(amax, fmt_max);
+  return s == 0.0f ? 1.0f : s;
+}
+
+__device__ __forceinline__ void store_codes4(uint8_t* q, int64_t off, int64_t col, int64_t cols,
+                                             bool vec_ok, uint32_t codes) {
+  if (vec_ok && col + 3 < cols) {
+    *reinterpret_cast<uint32_t*>(q + off) = codes;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (col + j < cols) q[off + j] = static_cast<uint8_t>(codes >> (8 * j));
+  }
+}
+
+// One CTA per 128 x 128 tile; 256 threads, thread t owns columns 4*(t%32)..+3
+// of rows t/32 + 8i, i < 16.
+template <bool kBF16>
+__global__ void __launch_bounds__(256) quantize_fp8_tile_kernel(
+    const void* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, int fmt, float fmt_max,
+    bool vec_in, bool vec_out, uint8_t* __restrict__ q, float* __restrict__ scales) {
+  __shared__ float warp_max[8];
+  __shared__ float tile_scale;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
+  const int cg = threadIdx.x & 31;
+  const int rr = threadIdx.x >> 5;
+  const int64_t col = c0 + 4 * cg;
+  float v[16][4];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int64_t row = r0 + rr + 8 * i;
+    if (row < rows && col < cols) {
+      load4<kBF16>(x, row, col, cols, ld, vec_in, v[i]);
+    } else {
+      v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fabsf(v[i][j]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (cg == 0) warp_max[rr] = amax;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = warp_max[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, warp_max[w]);
+    const float s = fp8_scale(m, fmt_max);
+    tile_scale = s;
+    scales[static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x] = s;
+  }
+  __syncthreads();
+  const float s = tile_scale;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int64_t row = r0 + rr + 8 * i;
+    if (row < rows && col < cols) {
+      const uint32_t c = cvt4_fp8(fmt, __fdiv_rn(v[i][0], s), __fdiv_rn(v[i][1], s),
+                                  __fdiv_rn(v[i][2], s), __fdiv_rn(v[i][3], s));
+      store_codes4(q, row * cols + col, col, cols, vec_out, c);
+    }
+  }
+}
+
+// One warp per (row, 128-wide K tile); each warp takes 4 consecutive items.
+// Scales stored K-tile major: scales[t * rows + row].
+template <bool kBF16>
+__global__ void __launch_bounds__(256) quantize_fp8_row_kernel(
+    const void* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, int fmt, float fmt_max,
+    bool vec_in, bool vec_out, uint8_t* __restrict__ q, float* __restrict__ scales) {
+  constexpr int kItems = 4;
+  const int64_t kt = (cols + 127) / 128;
+  const int64_t total = rows * kt;
+  const int64_t first = (static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * kItems;
+  const int lane = threadIdx.x & 31;
+  float v[kItems][4];
+#pragma unroll
+  for (int i = 0; i < kItems; ++i) {
+    const int64_t it = first + i;
+    const int64_t row = it / kt, t = it % kt;
+    const int64_t col = t * 128 + 4 * lane;
+    if (it < total && col < cols) {
+      load4<kBF16>(x, row, col, cols, ld, vec_in, v[i]);
+    } else {
+      v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.0f;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kItems; ++i) {
+    const int64_t it = first + i;
+    if (it >= total) break;  // uniform across the warp
+    float amax = fmaxf(fmaxf(fabsf(v[i][0]), fabsf(v[i][1])), fmaxf(fabsf(v[i][2]), fabsf(v[i][3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = fp8_scale(amax, fmt_max);
+    const int64_t row = it / kt, t = it % kt;
+    const int64_t col = t * 128 + 4 * lane;
+    if (lane == 0) scales[t * rows + row] = s;
+    if (col < cols) {
+      const uint32_t c = cvt4_fp8(fmt, __fdiv_rn(v[i][0], s), __fdiv_rn(v[i][1], s),
+                                  __fdiv_rn(v[i][2], s), __fdiv_rn(v[i][3], s));
+      store_codes4(q, row * cols + col, col, cols, vec_out, c);
+    }
+  }
+}
+
+// E8M0 code of the power of two nearest to v >= 0 (ties up), from v's bits.
+__device__ __forceinline__ uint32_t e8m0_nearest(float v) {
+  const uint32_t b = __float_as_uint(v);
+  const int ef = static_cast<int>((b >> 23) & 0xFFu);
+  const uint32_t mf = b & 0x7FFFFFu;
+  int e;
+  if (ef != 0) {
+    e = ef - 127 + (mf >= 0x400000u ? 1 : 0);
+  } else if (mf == 0) {
+    return 127u;  // v == 0
+  } else {
+    const int p = 31 - __clz(mf);  // leading one of the subnormal significand
+    e = p - 149 + ((p >= 1 && ((mf >> (p - 1)) & 1u)) ? 1 : 0);
+  }
+  e += 127;
+  return static_cast<uint32_t>(e < 0 ? 0 : (e > 254 ? 254 : e));
+}
+
+__device__ __forceinline__ uint32_t cvt2_e2m1(float first, float second) {
+  uint32_t r;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}\n"
+      : "=r"(r)
+      : "f"(second), "f"(first));
+  return r & 0xFFu;
+}
+
+__device__ __forceinline__ int64_t sf_tc_offset(int64_t row, int64_t b, int64_t kb_groups) {
+  return ((row >> 7) * kb_groups + (b >> 2)) * 512 + (row & 31) * 16 + ((row & 127) >> 5) * 4 +
+         (b & 3);
+}
+
+// One warp per (row, 256-column chunk); lane l owns 8 elements, 4 lanes per
+// 32-element block.  In the tcgen05 layout the grid also covers the padding
+// rows / K-blocks of the last atoms and writes 127 there.
+template <bool kBF16, bool kTC>
+__global__ void __launch_bounds__(256) quantize_mxfp4_kernel(
+    const void* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, bool vec_in,
+    uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  const int64_t kb = cols / 32;
+  const int64_t kb_pad = kTC ? ((kb + 3) / 4) * 4 : kb;
+  const int64_t chunks = (kb_pad + 7) / 8;
+  const int64_t rows_pad = kTC ? ((rows + 127) / 128) * 128 : rows;
+  const int64_t w = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (w >= rows_pad * chunks) return;
+  const int64_t row = w / chunks, chunk = w % chunks;
+  const int lane = threadIdx.x & 31;
+  const int64_t b = chunk * 8 + (lane >> 2);
+  const int64_t col = b * 32 + (lane & 3) * 8;
+  const bool data = row < rows && b < kb;
+  float v[8];
+  if (data) {
+    load4<kBF16>(x, row, col, cols, ld, vec_in, *reinterpret_cast<float(*)[4]>(&v[0]));
+    load4<kBF16>(x, row, col + 4, cols, ld, vec_in, *reinterpret_cast<float(*)[4]>(&v[4]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const uint32_t code = e8m0_nearest(__fdiv_rn(amax, 6.0f));
+  if (data) {
+    // 2^-(code-127) as an FP32 normal: code in [0,254] -> exponent field 254-code
+    const float inv = __uint_as_float(static_cast<uint32_t>(254 - static_cast<int>(code)) << 23);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      packed |= cvt2_e2m1(v[2 * j] * inv, v[2 * j + 1] * inv) << (8 * j);
+    *reinterpret_cast<uint32_t*>(q + row * (cols / 2) + col / 2) = packed;
+  }
+  if ((lane & 3) == 0 && b < kb_pad) {
+    const uint8_t c = data ? static_cast<uint8_t>(code) : static_cast<uint8_t>(127);
+    if (kTC) {
+      sf[sf_tc_offset(row, b, kb_pad / 4)] = c;
+    } else if (data) {
+      sf[row * kb + b] = c;
+    }
+  }
+}
+
+__global__ void sf_to_tcgen05_kernel(const uint8_t* __restrict__ sf, int64_t rows, int64_t kb,
+                                     int64_t total, uint8_t* __restrict__ out) {
+  const int64_t off = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (off >= total) return;
+  const int64_t groups = (kb + 3) / 4;
+  const int64_t atom = off / 512, within = off % 512;
+  const int64_t rb = atom / groups, cb = atom % groups;
+  const int64_t r = rb * 128 + ((within % 16) / 4) * 32 + within / 16;
+  const int64_t c = cb * 4 + within % 4;
+  out[off] = (r < rows && c < kb) ? sf[r * kb + c] : static_cast<uint8_t>(127);
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+cudaError_t quantize_error_read_and_clear(cudaStream_t s, uint32_t* out) {
+  uint32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_quant_error, sizeof(uint32_t), 0,
+                                            cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyToSymbolAsync(g_quant_error, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(s);
+}
+
+cudaError_t launch_quantize_fp8_tile(const void* x, bool src_bf16, int64_t rows, int64_t cols,
+                                     int64_t ld, int fmt, float fmt_max, uint8_t* q,
+                                     float* scales, cudaStream_t s) {
+  const bool vec_in = src_bf16 ? (aligned(x, 8) && ld % 4 == 0) : (aligned(x, 16) && ld % 4 == 0);
+  const bool vec_out = aligned(q, 4) && cols % 4 == 0;
+  dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>((rows + 127) / 128));
+  if (src_bf16)
+    quantize_fp8_tile_kernel<true><<<grid, 256, 0, s>>>(x, rows, cols, ld, fmt, fmt_max, vec_in,
+                                                         vec_out, q, scales);
+  else
+    quantize_fp8_tile_kernel<false><<<grid, 256, 0, s>>>(x, rows, cols, ld, fmt, fmt_max, vec_in,
+                                                          vec_out, q, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_fp8_row(const void* x, bool src_bf16, int64_t rows, int64_t cols,
+                                    int64_t ld, int fmt, float fmt_max, uint8_t* q, float* scales,
+                                    cudaStream_t s) {
+  const bool vec_in = src_bf16 ? (aligned(x, 8) && ld % 4 == 0) : (aligned(x, 16) && ld % 4 == 0);
+  const bool vec_out = aligned(q, 4) && cols % 4 == 0;
+  const int64_t items = rows * ((cols + 127) / 128);
+  const int64_t blocks = (items + 31) / 32;  // 8 warps x 4 items
+  if (src_bf16)
+    quantize_fp8_row_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        x, rows, cols, ld, fmt, fmt_max, vec_in, vec_out, q, scales);
+  else
+    quantize_fp8_row_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        x, rows, cols, ld, fmt, fmt_max, vec_in, vec_out, q, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_mxfp4(const void* x, bool src_bf16, int64_t rows, int64_t cols,
+                                  int64_t ld, uint8_t* q, uint8_t* sf, bool tc_layout,
+                                  cudaStream_t s) {
+  const bool vec_in = src_bf16 ? (aligned(x, 8) && ld % 4 == 0) : (aligned(x, 16) && ld % 4 == 0);
+  const int64_t kb = cols / 32;
+  const int64_t kb_pad = tc_layout ? ((kb + 3) / 4) * 4 : kb;
+  const int64_t rows_pad = tc_layout ? ((rows + 127) / 128) * 128 : rows;
+  const int64_t warps = rows_pad * ((kb_pad + 7) / 8);
+  const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
+  if (src_bf16) {
+    if (tc_layout)
+      quantize_mxfp4_kernel<true, true><<<blocks, 256, 0, s>>>(x, rows, cols, ld, vec_in, q, sf);
+    else
+      quantize_mxfp4_kernel<true, false><<<blocks, 256, 0, s>>>(x, rows, cols, ld, vec_in, q, sf);
+  } else {
+    if (tc_layout)
+      quantize_mxfp4_kernel<false, true><<<blocks, 256, 0, s>>>(x, rows, cols, ld, vec_in, q, sf);
+    else
+      quantize_mxfp4_kernel<false, false><<<blocks, 256, 0, s>>>(x, rows, cols, ld, vec_in, q, sf);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sf_to_tcgen05(const uint8_t* sf, int64_t rows, int64_t kblocks, uint8_t* out,
+                                 cudaStream_t s) {
+  const int64_t total = ((rows + 127) / 128) * ((kblocks + 3) / 4) * 512;
+  sf_to_tcgen05_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, s>>>(
+      sf, rows, kblocks, total, out);
+  return cudaGetLastError();
+}
+
+}  // namespace bsg

@@ -1,0 +1,202 @@
+/*
+ * bsg.h - block-scaled low-precision GEMM on GB300 (sm_103a): the C ABI of
+ * libbsg.so.
+ *
+ * The library computes
+ *
+ *     D = sum_k (s_A a_k)(s_B b_k) + C          (FP32 accumulation)
+ *
+ * for FP8 operands (E4M3 / E5M2) with per-tile FP32 scales and for MXFP4
+ * operands (E2M1 values, one E8M0 power-of-two scale per 32 elements along K),
+ * and the quantisers that produce those operands from FP32 or BF16 sources.
+ *
+ * Sources of the operations (web pages on the subject; each entry point below
+ * names its passage):
+ *   "FP8 GEMM on CDNA4"          - per-tile scale max_abs/448, FP32 accumulation,
+ *                                  write-back times s_A*s_B (sections 2.2, 3.3, 4.2, 4.4)
+ *   "Rubin FP4 GEMM deep dive"   - MXFP4: E2M1, E8M0 per 32 along K, nibble order,
+ *                                  A row-major / B column-major (sections 2.1-2.2, 3.1-3.4, 4.2)
+ *   "FP8 MMA internals on Hopper"- why per-K-tile promotion into an FP32
+ *                                  accumulator is needed
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument named as a device buffer is a CUDA device pointer
+ *     on the current device; the caller allocates and owns it.  The library
+ *     never allocates device memory and never frees a caller's buffer.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every compute call is asynchronous on that stream; buffers
+ *     must stay alive until the stream has passed the call.
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid call returns an error status and launches nothing.
+ *   - Device-side failures (a bounded wait that ran out) never trap: the
+ *     kernel records them in a device error word and returns; read it with
+ *     bsg_device_error().
+ *   - Matrices are row-major with a leading dimension in elements unless a
+ *     comment says otherwise.  Operand B of a GEMM is K x N column-major,
+ *     i.e. stored as N rows of K contiguous elements (N x K row-major).
+ */
+#ifndef BSG_H_
+#define BSG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BSG_OK = 0,
+  BSG_ERR_INVALID_ARG = 1,   /* null pointer, negative or zero size, bad enum        */
+  BSG_ERR_UNSUPPORTED = 2,   /* format / granularity / dtype combination not offered */
+  BSG_ERR_ALIGNMENT = 3,     /* pointer or leading dimension not 16-byte aligned     */
+  BSG_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch, attribute, ...)  */
+  BSG_ERR_TIMEOUT = 5,       /* a device-side bounded wait ran out (bsg_device_error) */
+  BSG_ERR_WORKSPACE = 6      /* workspace missing or smaller than bsg_gemm_workspace_size */
+} bsg_status;
+
+typedef enum {
+  BSG_E4M3 = 0,              /* FP8, 4-bit exponent, 3-bit mantissa, "fn": max 448, no Inf */
+  BSG_E5M2 = 1,              /* FP8, 5-bit exponent, 2-bit mantissa, max 57344            */
+  BSG_E2M1 = 2               /* FP4, values {0,.5,1,1.5,2,3,4,6} with sign, 2 per byte,
+                                first element in the low nibble                            */
+} bsg_format;
+
+typedef enum {
+  BSG_F32 = 0,
+  BSG_BF16 = 1
+} bsg_dtype;
+
+typedef enum {
+  /* One FP32 scale per 128 x 128 tile.  Scale array [ceil(R/128)][ceil(C/128)]
+     row-major, R = rows of the quantised matrix, C = its K extent.           */
+  BSG_SCALE_TILE128x128 = 0,
+  /* One FP32 scale per 1 x 128 run of a row.  Stored K-tile major:
+     [ceil(C/128)][R], so the scales of one K tile are contiguous.            */
+  BSG_SCALE_ROW1x128 = 1,
+  /* One E8M0 scale per 1 x 32 block along K (MXFP4); layout per bsg_sf_layout */
+  BSG_SCALE_BLOCK1x32_E8M0 = 2
+} bsg_scale_gran;
+
+typedef enum {
+  /* Canonical E8M0 layout: [R][C/32] bytes, row-major.                        */
+  BSG_SF_ROWMAJOR = 0,
+  /* The order the block-scaled tensor-core MMA reads scales in: 512-byte
+     atoms ordered by (row block of 128, group of 4 K-blocks); inside an atom
+     the byte of row r, K-block c is at (r%32)*16 + ((r%128)/32)*4 + (c%4).
+     Size ceil(R/128) * ceil(C/128) * 512 bytes; padding bytes hold 127 (1.0).
+     bsg_gemm reads MXFP4 scales in this layout only.                          */
+  BSG_SF_TCGEN05 = 1
+} bsg_sf_layout;
+
+/* ------------------------------------------------------------------------ */
+/* bsg_quantize_fp8 - per-tile FP8 quantisation.
+ *
+ * "FP8 GEMM on CDNA4", section 3.3 (scale = max_abs / 448, each element divided
+ * by the scale and stored as FP8) and section 4.2 (warp-level max reduction).
+ * For each scale group G (a 128 x 128 tile or a 1 x 128 run, per `gran`):
+ *     s_G = max_{x in G} |x| / fmt_max       (FP32, round to nearest; 1.0 if 0)
+ *     q   = RNE_satfinite_fmt(x / s_G)       (IEEE FP32 division)
+ *
+ * x        device, rows x cols source, leading dimension `ld` elements,
+ *          FP32 or BF16 per `src`.  Finite values only.
+ * fmt      BSG_E4M3 or BSG_E5M2.
+ * gran     BSG_SCALE_TILE128x128 or BSG_SCALE_ROW1x128.
+ * fmt_max  the value the group maximum maps to; 0 selects the format's own
+ *          maximum (448 for E4M3, 57344 for E5M2).  Must be >= 0 and finite.
+ * q        device, rows x cols codes, leading dimension `cols` bytes.
+ * scales   device, FP32 scales in the layout `gran` describes.
+ * Errors: BSG_ERR_INVALID_ARG (null, rows/cols <= 0, ld < cols, bad fmt_max),
+ *         BSG_ERR_UNSUPPORTED (fmt or gran not FP8), BSG_ERR_CUDA.
+ */
+bsg_status bsg_quantize_fp8(const void* x, bsg_dtype src, int64_t rows, int64_t cols,
+                            int64_t ld, bsg_format fmt, bsg_scale_gran gran, float fmt_max,
+                            uint8_t* q, float* scales, void* stream);
+
+/* bsg_quantize_mxfp4 - MXFP4 quantisation.
+ *
+ * "Rubin FP4 GEMM deep dive", section 4.2 steps 1-3: per block of 32
+ * consecutive elements along a row, v = max|x| / 6 (FP32); the E8M0 scale is
+ * the power of two nearest to v (linear distance, a tie goes to the larger;
+ * v = 0 gives 1.0; codes clamp to [0, 254]); each element is multiplied by the
+ * inverse power of two (exact) and rounded to E2M1 (nearest, ties to even,
+ * saturating at 6); two codes per byte, first element in the low nibble.
+ *
+ * x        device, rows x cols source (FP32 or BF16), leading dimension `ld`.
+ * cols     K extent, a multiple of 32.
+ * q_packed device, rows x cols/2 bytes, leading dimension cols/2.
+ * sf       device, E8M0 scales in `layout` (bsg_scale_bytes gives the size).
+ * Errors: BSG_ERR_INVALID_ARG (null, sizes, cols % 32), BSG_ERR_CUDA.
+ */
+bsg_status bsg_quantize_mxfp4(const void* x, bsg_dtype src, int64_t rows, int64_t cols,
+                              int64_t ld, uint8_t* q_packed, uint8_t* sf,
+                              bsg_sf_layout layout, void* stream);
+
+/* bsg_gemm - block-scaled GEMM D = sum_k (s_A a_k)(s_B b_k) + C.
+ *
+ * "FP8 GEMM on CDNA4", sections 2.2 (FP32 accumulation), 3.3 and 4.4 (the
+ * accumulated result is multiplied by s_A * s_B); "Rubin FP4 GEMM deep dive",
+ * sections 2.2 and 3.1 (K-blocked scaling: each K block's partial sum is
+ * multiplied by its two scales before it is accumulated).  FP8 scales are not
+ * powers of two, so the FP8 path multiplies each 128-wide K tile's partial
+ * sum by s_A * s_B and adds it into an FP32 accumulator (the per-K-tile
+ * promotion "FP8 MMA internals on Hopper" motivates).  MXFP4 scales are
+ * applied by the tensor core.
+ *
+ * A   device, M x K codes, row-major: FP8 one byte per element (leading
+ *     dimension K bytes), E2M1 packed (K/2 bytes per row).
+ * B   device, K x N column-major = N x K row-major, same encoding rules.
+ * fa, fb  operand formats: both FP8 (E4M3 / E5M2, any mix) or both E2M1.
+ * sA, ga  A's scales: FP8 -> BSG_SCALE_TILE128x128 ([ceil(M/128)][ceil(K/128)])
+ *         or BSG_SCALE_ROW1x128 ([ceil(K/128)][M]); E2M1 ->
+ *         BSG_SCALE_BLOCK1x32_E8M0 in the BSG_SF_TCGEN05 layout.
+ * sB, gb  B's scales, same rules with N in place of M.
+ * C   device, optional (NULL) FP32 M x N row-major addend.
+ * D   device, M x N row-major output, FP32 or BF16 (round to nearest even).
+ * workspace, workspace_bytes
+ *     device scratch of at least bsg_gemm_workspace_size(...) bytes (may be
+ *     NULL when that size is 0).  It must be zero-filled before its first use;
+ *     the library leaves it zero-filled after every successful call.  Calls
+ *     that share a workspace must not overlap in time.
+ * Constraints: M, N, K > 0; K % 16 == 0 for FP8, K % 32 == 0 for E2M1; A, B,
+ *     D, C 16-byte aligned.
+ * Errors: BSG_ERR_INVALID_ARG, BSG_ERR_UNSUPPORTED, BSG_ERR_ALIGNMENT,
+ *         BSG_ERR_WORKSPACE, BSG_ERR_CUDA.
+ */
+bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K,
+                    const void* A, bsg_format fa, const void* sA, bsg_scale_gran ga,
+                    const void* B, bsg_format fb, const void* sB, bsg_scale_gran gb,
+                    const float* C, void* D, bsg_dtype out,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace bsg_gemm needs for this problem (0 if none). */
+size_t bsg_gemm_workspace_size(int64_t M, int64_t N, int64_t K, bsg_format fa, bsg_format fb);
+
+/* Bytes of the scale array of a rows x cols matrix for a granularity and,
+ * for E8M0 scales, a layout (the layout is ignored for FP32 scales). */
+size_t bsg_scale_bytes(int64_t rows, int64_t cols, bsg_scale_gran gran, bsg_sf_layout layout);
+
+/* bsg_sf_to_tcgen05 - rewrite row-major E8M0 scales [rows][kblocks] into the
+ * BSG_SF_TCGEN05 layout (a permutation plus padding with 127).
+ * sf_rowmajor, sf_tc: device buffers; sf_tc holds
+ * bsg_scale_bytes(rows, 32*kblocks, BSG_SCALE_BLOCK1x32_E8M0, BSG_SF_TCGEN05). */
+bsg_status bsg_sf_to_tcgen05(const uint8_t* sf_rowmajor, int64_t rows, int64_t kblocks,
+                             uint8_t* sf_tc, void* stream);
+
+/* Human-readable name of a status. */
+const char* bsg_status_string(bsg_status status);
+
+/* Synchronise `stream`, then read and clear the device error word.  Returns
+ * BSG_OK, BSG_ERR_TIMEOUT if a kernel's bounded wait ran out since the last
+ * call, or BSG_ERR_CUDA if the synchronisation itself failed. */
+bsg_status bsg_device_error(void* stream);
+
+/* Number of SMs of the current device the library sizes persistent grids by
+ * (0 if the query fails). */
+int bsg_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSG_H_ */
