@@ -15,13 +15,21 @@
 // lives in tensor memory, double-buffered, so the MMA of tile t+1 overlaps
 // the drain of tile t.
 //
-// Warp roles (320 threads, one CTA per SM, persistent over output tiles):
-//   warps 0-7  promotion + epilogue.  Warp w reads TMEM lanes 32*(w%4)..+31
-//              (its rows) and column half w/4 of the 256-wide tile.
-//   warp 8     producer: TMA loads of A (128 x 128 B) and B (256 x 128 B)
+// Warp roles (384 threads = 3 warpgroups, one CTA per SM, persistent over
+// output tiles):
+//   warp 0     producer: TMA loads of A (128 x 128 B) and B (256 x 128 B)
 //              into a 4-stage ring; cp.async of the K tile's scales into an
 //              8-slot scale ring.
-//   warp 9     tensor-memory allocator and MMA issuer (one elected lane).
+//   warp 1     tensor-memory allocator and MMA issuer (one lane).
+//   warps 2-3  idle (they complete warpgroup 0).
+//   warps 4-11 promotion + epilogue: warpgroups 1 and 2.  Warp w reads TMEM
+//              lanes 32*(w%4)..+31 (its rows) and column half (w-4)/4 of the
+//              256-wide tile.
+// Registers: the kernel launches at 168 per thread (384 x 168 = 64512);
+// warpgroup 0 gives back down to 40 and the promotion warpgroups take 232
+// each, 128 x 40 + 256 x 232 = 64512, which holds 128 FP32 accumulators plus
+// two 32-column TMEM load buffers per thread without spilling.  The drain
+// uses paired FP32 FMAs (fma.rn.f32x2), one instruction per two elements.
 // Every wait is bounded; a wait that runs out sets the error word, raises a
 // CTA-wide abort flag and all roles unwind to the final barrier.
 #include "common.cuh"
@@ -37,9 +45,14 @@ constexpr int BN = 256;
 constexpr int BK = 128;            // one scale tile along K = one promotion unit
 constexpr int kStages = 4;
 constexpr int kScaleSlots = 8;
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kFirstPromoWarp = 4;
+constexpr int kRegsSmall = 56;     // warpgroup 0 after setmaxnreg.dec
+constexpr int kRegsLarge = 224;    // promotion warpgroups after setmaxnreg.inc
+static_assert(128 * kRegsSmall + 256 * kRegsLarge <= kThreads * 168,
+              "register split exceeds the launch allocation");
 constexpr int kTmemCols = 512;     // two 256-column FP32 partial buffers
 constexpr int kGroupM = 8;         // tile raster: groups of 8 M tiles
 
@@ -126,6 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
+    setmaxnreg_dec<kRegsSmall>();
     uint32_t it = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
@@ -180,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
+    setmaxnreg_dec<kRegsSmall>();
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
@@ -212,19 +227,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(smem_u32(&sm.final_bar), 0)) raise_abort(sm);
     }
     __syncwarp();
+  } else if (warp < kFirstPromoWarp) {
+    setmaxnreg_dec<kRegsSmall>();            // idle warps of warpgroup 0
   } else {
     // ------------------------------------------------- promotion + epilogue
-    const int q = warp & 3;          // TMEM lane quarter = rows 32q..32q+31
-    const int g = warp >> 2;         // column half of the 256-wide tile
+    setmaxnreg_inc<kRegsLarge>();
+    const int q = warp & 3;                        // TMEM lane quarter = rows 32q..32q+31
+    const int g = (warp - kFirstPromoWarp) >> 2;   // column half of the 256-wide tile
     const int row = q * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + g * 128;
     uint32_t it = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
       const TileCoord tc = tile_coord(t, num_m, num_n);
-      float acc[128];
+      uint64_t acc[64];                            // 128 FP32 accumulators, in pairs
 #pragma unroll
-      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < 64; ++j) acc[j] = 0ull;
       for (int kt = 0; kt < KT; ++kt, ++it) {
         const uint32_t b = it & 1u;
         const uint32_t tph = (it >> 1) & 1u;
@@ -239,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const float sa = kARow ? sm.sa[ss][row] : sm.sa[ss][0];
         const float sc = kBRow ? sa : sa * sm.sb[ss][g * 128];
+        const uint64_t sc2 = f32x2_pack(sc, sc);
         const uint32_t taddr = lane_base + b * BN;
         uint32_t r0[16], r1[16];
         tmem_ld_16(taddr, r0);
@@ -249,9 +268,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t (&nxt)[16] = (c & 1) ? r0 : r1;
           if (c + 1 < 8) tmem_ld_16(taddr + (c + 1) * 16, nxt);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float scj = kBRow ? sc * sm.sb[ss][g * 128 + c * 16 + j] : sc;
-            acc[c * 16 + j] = fmaf(scj, __uint_as_float(cur[j]), acc[c * 16 + j]);
+          for (int j = 0; j < 8; ++j) {
+            const uint64_t p = f32x2_pack(__uint_as_float(cur[2 * j]), __uint_as_float(cur[2 * j + 1]));
+            if (kBRow) {
+              const float2 sbv = *reinterpret_cast<const float2*>(&sm.sb[ss][g * 128 + c * 16 + 2 * j]);
+              ffma2(acc[c * 8 + j], fmul2(sc2, f32x2_pack(sbv.x, sbv.y)), p);
+            } else {
+              ffma2(acc[c * 8 + j], sc2, p);
+            }
           }
           if (c + 1 < 8) tc_wait_ld_16(nxt);
         }
@@ -263,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      // ---- epilogue: rows of this thread, 128 columns of its half
+      // ---- epilogue: this thread's row, 128 columns of its half
       const int64_t grow = static_cast<int64_t>(tc.m) * BM + row;
       const int gcol0 = tc.n * BN + g * 128;
       if (grow < M) {
@@ -274,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col = gcol0 + c;
             float v[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = acc[c + j];
+            for (int j = 0; j < 4; ++j) f32x2_unpack(acc[c / 2 + j], v[2 * j], v[2 * j + 1]);
             if (Cin != nullptr) {
 #pragma unroll
               for (int j = 0; j < 8; ++j)
@@ -298,7 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 128; c += 4) {
             const int col = gcol0 + c;
-            float v[4] = {acc[c], acc[c + 1], acc[c + 2], acc[c + 3]};
+            float v[4];
+            f32x2_unpack(acc[c / 2], v[0], v[1]);
+            f32x2_unpack(acc[c / 2 + 1], v[2], v[3]);
             if (Cin != nullptr) {
 #pragma unroll
               for (int j = 0; j < 4; ++j)
