@@ -61,6 +61,7 @@ struct __align__(1024) Smem {
   uint8_t b[kStages][BN * BK];
   float sa[kScaleSlots][BM];
   float sb[kScaleSlots][BN];
+  uint8_t epi[8][32 * 64];   // per promotion warp: 32 rows x 64 B output staging
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t tfull[2];
@@ -76,13 +77,21 @@ struct TileCoord {
   int m, n;
 };
 
-__device__ __forceinline__ TileCoord tile_coord(int t, int num_m, int num_n) {
-  const int group_size = kGroupM * num_n;
+// Raster of the persistent tile loop.  Tiles are visited in groups of
+// kGroupM rows of tiles along one dimension while the other is swept, so the
+// operand panel of the group stays in L2 and the swept operand is re-read
+// from L2.  along_n = true groups along N (sweeps M): chosen when A is the
+// smaller operand, so the whole of A is what gets re-read and stays resident.
+__device__ __forceinline__ TileCoord tile_coord(int t, int num_m, int num_n, bool along_n) {
+  const int outer = along_n ? num_n : num_m;
+  const int inner = along_n ? num_m : num_n;
+  const int group_size = kGroupM * inner;
   const int group = t / group_size;
-  const int first_m = group * kGroupM;
-  const int gsz = min(num_m - first_m, kGroupM);
+  const int first = group * kGroupM;
+  const int gsz = min(outer - first, kGroupM);
   const int local = t % group_size;
-  return {first_m + local % gsz, local / gsz};
+  const int o = first + local % gsz, i = local / gsz;
+  return along_n ? TileCoord{i, o} : TileCoord{o, i};
 }
 
 __device__ __forceinline__ void raise_abort(Smem& sm) {
@@ -95,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const float* __restrict__ sA, const float* __restrict__ sB,
                     const float* __restrict__ Cin, void* __restrict__ Dout, int M, int N, int K,
-                    uint32_t idesc, bool vec_out) {
+                    uint32_t idesc, bool vec_out, bool raster_n) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~static_cast<uintptr_t>(1023));
@@ -140,10 +149,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     setmaxnreg_dec<kRegsSmall>();
+    const uint64_t keep = l2_policy_evict_last();   // operands are re-read by other tiles
     uint32_t it = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-      const TileCoord tc = tile_coord(t, num_m, num_n);
+      const TileCoord tc = tile_coord(t, num_m, num_n, raster_n);
       for (int kt = 0; kt < KT; ++kt, ++it) {
         if (sm.abort_flag) { ok = false; break; }
         const int s = static_cast<int>(it % kStages);
@@ -157,8 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (good) {
             const uint32_t fb = smem_u32(&sm.full[s]);
             mbar_arrive_expect_tx(fb, (BM + BN) * BK);
-            tma_load_2d(smem_u32(sm.a[s]), &tmA, fb, kt * BK, tc.m * BM);
-            tma_load_2d(smem_u32(sm.b[s]), &tmB, fb, kt * BK, tc.n * BN);
+            tma_load_2d_hint(smem_u32(sm.a[s]), &tmA, fb, kt * BK, tc.m * BM, keep);
+            tma_load_2d_hint(smem_u32(sm.b[s]), &tmB, fb, kt * BK, tc.n * BN, keep);
           } else {
             raise_abort(sm);
           }
@@ -236,10 +246,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = (warp - kFirstPromoWarp) >> 2;   // column half of the 256-wide tile
     const int row = q * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + g * 128;
+    const uint64_t stream_out = l2_policy_evict_first();   // the result is not re-read
     uint32_t it = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-      const TileCoord tc = tile_coord(t, num_m, num_n);
+      const TileCoord tc = tile_coord(t, num_m, num_n, raster_n);
       uint64_t acc[64];                            // 128 FP32 accumulators, in pairs
 #pragma unroll
       for (int j = 0; j < 64; ++j) acc[j] = 0ull;
@@ -287,58 +298,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      // ---- epilogue: this thread's row, 128 columns of its half
-      const int64_t grow = static_cast<int64_t>(tc.m) * BM + row;
+      // ---- epilogue.  Each thread holds one row x 128 columns.  The warp
+      // passes its 32 rows through a 32 x 64-byte staging buffer (16-byte
+      // pieces XOR-swizzled by row, so both phases are bank-conflict free)
+      // and writes back 8 rows x 64 contiguous bytes per store instruction
+      // instead of 32 scattered 16-byte pieces.
+      const int64_t row0 = static_cast<int64_t>(tc.m) * BM + q * 32;
       const int gcol0 = tc.n * BN + g * 128;
-      if (grow < M) {
-        if (kBF16Out) {
-          __nv_bfloat16* D = static_cast<__nv_bfloat16*>(Dout) + grow * N;
+      const uint32_t stage = smem_u32(sm.epi[warp - kFirstPromoWarp]);
+      constexpr int kElem = kBF16Out ? 2 : 4;
+      constexpr int kColsPerChunk = 64 / kElem;     // 32 (BF16) or 16 (FP32)
+      constexpr int kPerPiece = 16 / kElem;         // values per 16-byte piece
+      const int64_t my_row = row0 + lane;
 #pragma unroll
-          for (int c = 0; c < 128; c += 8) {
-            const int col = gcol0 + c;
-            float v[8];
+      for (int ch = 0; ch < 128 / kColsPerChunk; ++ch) {
+        const int col0 = gcol0 + ch * kColsPerChunk;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) f32x2_unpack(acc[c / 2 + j], v[2 * j], v[2 * j + 1]);
-            if (Cin != nullptr) {
+        for (int p = 0; p < 4; ++p) {
+          float v[kPerPiece];
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                if (col + j < N) v[j] += __ldg(Cin + grow * N + col + j);
-            }
-            if (vec_out && col + 7 < N) {
-              uint4 u;
-              u.x = pack_bf16x2(v[0], v[1]);
-              u.y = pack_bf16x2(v[2], v[3]);
-              u.z = pack_bf16x2(v[4], v[5]);
-              u.w = pack_bf16x2(v[6], v[7]);
-              *reinterpret_cast<uint4*>(D + col) = u;
-            } else {
+          for (int j = 0; j < kPerPiece / 2; ++j)
+            f32x2_unpack(acc[(ch * kColsPerChunk + p * kPerPiece) / 2 + j], v[2 * j], v[2 * j + 1]);
+          if (Cin != nullptr && my_row < M) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                if (col + j < N) D[col + j] = __float2bfloat16_rn(v[j]);
+            for (int j = 0; j < kPerPiece; ++j) {
+              const int col = col0 + p * kPerPiece + j;
+              if (col < N) v[j] += __ldg(Cin + my_row * N + col);
             }
           }
-        } else {
-          float* D = static_cast<float*>(Dout) + grow * N;
+          uint4 u;
+          if (kBF16Out) {
+            u.x = pack_bf16x2(v[0], v[1]);
+            u.y = pack_bf16x2(v[2], v[3]);
+            u.z = pack_bf16x2(v[4 % kPerPiece], v[5 % kPerPiece]);
+            u.w = pack_bf16x2(v[6 % kPerPiece], v[7 % kPerPiece]);
+          } else {
+            u = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
+                           __float_as_uint(v[2 % kPerPiece]), __float_as_uint(v[3 % kPerPiece]));
+          }
+          st_shared_v4(stage + lane * 64 + ((p ^ ((lane >> 1) & 3)) << 4), u);
+        }
+        __syncwarp();
 #pragma unroll
-          for (int c = 0; c < 128; c += 4) {
-            const int col = gcol0 + c;
-            float v[4];
-            f32x2_unpack(acc[c / 2], v[0], v[1]);
-            f32x2_unpack(acc[c / 2 + 1], v[2], v[3]);
-            if (Cin != nullptr) {
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                if (col + j < N) v[j] += __ldg(Cin + grow * N + col + j);
-            }
-            if (vec_out && col + 3 < N) {
-              *reinterpret_cast<float4*>(D + col) = make_float4(v[0], v[1], v[2], v[3]);
+        for (int i = 0; i < 4; ++i) {
+          const int r = 8 * i + (lane >> 2);
+          const int p = lane & 3;
+          const uint4 u = ld_shared_v4(stage + r * 64 + ((p ^ ((r >> 1) & 3)) << 4));
+          const int64_t grow = row0 + r;
+          const int col = col0 + p * kPerPiece;
+          if (grow < M && col < N) {
+            if (vec_out && col + kPerPiece <= N) {
+              st_global_v4_hint(static_cast<uint8_t*>(Dout) + (grow * N + col) * kElem, u, stream_out);
             } else {
+              const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                if (col + j < N) D[col + j] = v[j];
+              for (int j = 0; j < kPerPiece; ++j) {
+                if (col + j >= N) break;
+                if (kBF16Out) {
+                  const uint16_t h = static_cast<uint16_t>(w[j / 2] >> (16 * (j % 2)));
+                  reinterpret_cast<uint16_t*>(Dout)[grow * N + col + j] = h;
+                } else {
+                  reinterpret_cast<float*>(Dout)[grow * N + col + j] = __uint_as_float(w[j]);
+                }
+              }
             }
           }
         }
+        __syncwarp();
       }
     }
   }
@@ -363,8 +389,10 @@ cudaError_t launch_variant(const Fp8GemmArgs& a, int num_sms, cudaStream_t s) {
   const uint32_t idesc = idesc_f8f6f4(static_cast<uint32_t>(a.afmt), static_cast<uint32_t>(a.bfmt), BM, BN);
   const bool vec_out = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) &&
                        (a.out_bf16 ? (a.N % 8 == 0) : (a.N % 4 == 0));
+  // keep the smaller operand resident: sweep it inside groups of the larger
+  const bool raster_n = static_cast<int64_t>(a.M) < static_cast<int64_t>(a.N);
   kern<<<grid, kThreads, smem, s>>>(a.tmA, a.tmB, a.sA, a.sB, a.C, a.D, a.M, a.N, a.K, idesc,
-                                    vec_out);
+                                    vec_out, raster_n);
   return cudaGetLastError();
 }
 
