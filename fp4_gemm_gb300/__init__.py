@@ -32,7 +32,7 @@ LAYOUT = {"rowmajor": 0, "tcgen05": 1}
 
 EXPORTS = ("bsg_quantize_fp8", "bsg_quantize_mxfp4", "bsg_gemm", "bsg_gemm_workspace_size",
            "bsg_scale_bytes", "bsg_sf_to_tcgen05", "bsg_status_string", "bsg_device_error",
-           "bsg_num_sms")
+           "bsg_num_sms", "bsg_gemm_decode_noalloc")
 
 
 class BsgError(RuntimeError):
@@ -73,6 +73,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsg_device_error.restype = i32
     lib.bsg_num_sms.argtypes = []
     lib.bsg_num_sms.restype = i32
+    lib.bsg_gemm_decode_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, vp, i32, vp]
+    lib.bsg_gemm_decode_noalloc.restype = i32
     _lib = lib
     return lib
 
@@ -220,4 +222,24 @@ def bsg_gemm(A: torch.Tensor, fa: str, sA: torch.Tensor, ga: str,
                         _ptr(sB), GRAN[gb], _ptr(C), _ptr(D), DTYPE[out], _ptr(workspace),
                         0 if workspace is None else workspace.numel(), _stream(stream)),
            "bsg_gemm")
+    return D
+
+
+def bsg_gemm_decode_noalloc(A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor, sB: torch.Tensor,
+                            C: torch.Tensor | None = None, out: str = "bf16",
+                            D: torch.Tensor | None = None, K: int | None = None, stream=None):
+    """The decode-shaped MXFP4 GEMM (M <= 32) using the library's built-in
+    scratch instead of a workspace: for callers that cannot allocate.  Calls
+    that overlap on the GPU race on that shared scratch."""
+    lib = load_library()
+    M, N = A.shape[0], B.shape[0]
+    if K is None:
+        K = A.shape[1] * 2
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.float32 if out == "f32" else torch.bfloat16,
+                        device=A.device)
+    _need_cuda(A, sA, B, sB, C, D)
+    _check(lib.bsg_gemm_decode_noalloc(M, N, K, _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(C),
+                                       _ptr(D), DTYPE[out], _stream(stream)),
+           "bsg_gemm_decode_noalloc")
     return D

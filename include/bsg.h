@@ -183,6 +183,28 @@ size_t bsg_scale_bytes(int64_t rows, int64_t cols, bsg_scale_gran gran, bsg_sf_l
 bsg_status bsg_sf_to_tcgen05(const uint8_t* sf_rowmajor, int64_t rows, int64_t kblocks,
                              uint8_t* sf_tc, void* stream);
 
+/* bsg_gemm_decode_noalloc - the decode-shaped MXFP4 GEMM (E2M1 x E2M1,
+ * M <= 32, same operands, scales, addend and output as bsg_gemm) without a
+ * caller-provided workspace.  The pages have no counterpart: this is an
+ * interface for callers that cannot allocate device memory, such as a
+ * plug-in that a serving runtime hands only its input and output buffers,
+ * or a decode loop that keeps cudaMalloc (which may synchronise the device
+ * and may fail) out of its steady state.
+ *
+ * Scratch: a fixed 8 MiB array compiled into the library's device image;
+ * every GPU that loads libbsg.so holds it until the process exits.  The
+ * first call on a device looks up the array's device address (with that
+ * device current), so make that first call before any stream capture.
+ * Each call clears the part it uses (an asynchronous memset on `stream`)
+ * and then runs the decode kernel; nothing is allocated.  All calls share
+ * the one array: calls whose execution overlaps on the GPU (different
+ * streams, or different host threads) race and give wrong results.
+ * Errors: as bsg_gemm; BSG_ERR_UNSUPPORTED if M > 32; BSG_ERR_WORKSPACE if
+ * the problem needs more scratch than 8 MiB (bsg_gemm_workspace_size tells). */
+bsg_status bsg_gemm_decode_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* sA,
+                                   const void* B, const void* sB, const float* C, void* D,
+                                   bsg_dtype out, void* stream);
+
 /* Human-readable name of a status. */
 const char* bsg_status_string(bsg_status status);
 
