@@ -33,21 +33,6 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D byte matrix `rows` x `inner_bytes` with a row pitch, loaded in boxes of
-// box_rows x 128 bytes with 128-byte swizzling; out-of-range reads are 0.
-bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
-                     uint64_t pitch, uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {inner_bytes, rows};
-  cuuint64_t strides[1] = {pitch};
-  cuuint32_t box[2] = {128, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int num_sms_current() {
   static int cache[64] = {0};
   int dev = 0;
@@ -75,6 +60,39 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 constexpr int64_t kDecodeMaxM = 32;
 
 }  // namespace
+
+namespace bsg {
+
+bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
+                     uint64_t pitch, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner_bytes, rows};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_kmajor_map_chunked(CUtensorMap* map, const void* base, uint64_t inner_bytes,
+                             uint64_t rows, uint64_t pitch, uint32_t box_rows,
+                             uint32_t box_chunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || inner_bytes % 128 != 0) return false;
+  cuuint64_t dims[3] = {128, rows, inner_bytes / 128};
+  cuuint64_t strides[2] = {pitch, 128};
+  cuuint32_t box[3] = {128, box_rows, box_chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace bsg
+
+using bsg::make_kmajor_map;
 
 extern "C" {
 
@@ -226,15 +244,14 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
     a.out_bf16 = out == BSG_BF16;
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
+    a.A = A;
+    a.B = B;
     if (M <= kDecodeMaxM) {
       const size_t need = bsg::gemm_mxfp4_decode_workspace(a.M, a.N, a.K, sms);
       if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)))
         return BSG_ERR_WORKSPACE;
-      // swap-AB: the weights (B, N rows) are the MMA's 128-row operand
-      const uint32_t xrows = M <= 16 ? 16 : 32;
-      if (!make_kmajor_map(&a.tmA, A, K / 2, M, K / 2, xrows) ||
-          !make_kmajor_map(&a.tmB, B, K / 2, N, K / 2, 128))
-        return BSG_ERR_CUDA;
+      // swap-AB: the weights (B, N rows) are the MMA's 128-row operand; the
+      // launcher encodes its own tensor maps
       return from_cuda(bsg::launch_gemm_mxfp4_decode(a, sms, s));
     }
     if (!make_kmajor_map(&a.tmA, A, K / 2, M, K / 2, 128) ||

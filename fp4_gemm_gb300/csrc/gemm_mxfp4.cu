@@ -289,22 +289,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------- decode path
 namespace decode {
 
-constexpr int kStages = 8;
 constexpr int kDecThreads = 192;   // warps 0-3 epilogue, 4 producer, 5 MMA
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kTmemCols = 256;
-constexpr int kSfColsPerStage = 16;
-constexpr int kSfBase = 64;        // after two accumulators of up to 32 columns
+constexpr int kTmemCols = 512;
+constexpr int kSlab = 128 * kRowBytes;   // one 128-row x 128-byte weight slab
+// Each MMA is tiny (M128 x N<=32 x K64); consecutive MMAs rotate over kAcc
+// independent accumulators so they do not form one dependent chain.  The
+// epilogue sums them.
+constexpr int kAcc = 4;
+// K chunks of 128 bytes (256 FP4 values) per pipeline stage when K allows the
+// chunked 3-D tensor map (K % 256 == 0): each TMA call then reads CH * 128
+// contiguous bytes of every weight row instead of 128.
+constexpr int kChunksWide = 2;
 
-template <int NX>
+template <int NX, int CH>
+struct Cfg {
+  static constexpr int kStageBytes = CH * (kSlab + NX * kRowBytes + 4 * kSfAtom);
+  static constexpr int kStages0 = (200 * 1024) / kStageBytes;
+  static constexpr int kStages = kStages0 > 10 ? 10 : kStages0;
+  static constexpr int kSfColsPerStage = CH * 16;   // per chunk: SFW 2 atoms + SFX 2 atoms
+  static constexpr int kAccCols = kAcc * NX;         // one buffer of accumulators
+  static constexpr int kSfBase = 2 * kAccCols;       // after the two buffers
+  static_assert(kSfBase + kStages * kSfColsPerStage <= kTmemCols, "TMEM columns");
+};
+
+template <int NX, int CH>
 struct __align__(1024) Smem {
-  uint8_t w[kStages][128 * kRowBytes];
-  uint8_t x[kStages][NX * kRowBytes];
-  uint8_t sfw[kStages][2 * kSfAtom];
-  uint8_t sfx[kStages][2 * kSfAtom];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  static constexpr int S = Cfg<NX, CH>::kStages;
+  uint8_t w[S][CH * kSlab];
+  uint8_t x[S][CH * NX * kRowBytes];
+  uint8_t sfw[S][CH * 2 * kSfAtom];
+  uint8_t sfx[S][CH * 2 * kSfAtom];
+  uint64_t full[S];
+  uint64_t empty[S];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t final_bar;
@@ -321,12 +339,16 @@ __host__ __device__ __forceinline__ int64_t owner(int64_t u, int64_t U, int64_t 
 
 struct Plan {
   int64_t tiles, KS, U, G, smax;
+  int ch;
 };
+
+int chunks_for(int K) { return (K % 256 == 0) ? kChunksWide : 1; }
 
 Plan make_plan(int N, int K, int num_sms) {
   Plan p;
+  p.ch = chunks_for(K);
   p.tiles = (N + 127) / 128;
-  p.KS = (static_cast<int64_t>(K) / 2 + kRowBytes - 1) / kRowBytes;
+  p.KS = (static_cast<int64_t>(K) / 2 + kRowBytes * p.ch - 1) / (kRowBytes * p.ch);
   p.U = p.tiles * p.KS;
   p.G = p.U < num_sms ? p.U : num_sms;
   p.smax = 1;
@@ -337,7 +359,7 @@ Plan make_plan(int N, int K, int num_sms) {
   return p;
 }
 
-template <int NX, bool kBF16Out>
+template <int NX, int CH, bool kBF16Out>
 __global__ void __launch_bounds__(kDecThreads, 1)
     gemm_mxfp4_decode_kernel(const __grid_constant__ CUtensorMap tmX,
                              const __grid_constant__ CUtensorMap tmW,
@@ -345,16 +367,21 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                              const float* __restrict__ Cin, void* __restrict__ Dout, int M, int N,
                              int K, int64_t KS, int64_t U, int64_t smax,
                              float* __restrict__ ws, uint32_t* __restrict__ counters) {
+  constexpr int kStages = Cfg<NX, CH>::kStages;
+  constexpr int kSfCols = Cfg<NX, CH>::kSfColsPerStage;
+  constexpr int kAccCols = Cfg<NX, CH>::kAccCols;
+  constexpr int kSfBase = Cfg<NX, CH>::kSfBase;
   extern __shared__ uint8_t smem_raw[];
-  Smem<NX>& sm = *reinterpret_cast<Smem<NX>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~static_cast<uintptr_t>(1023));
+  Smem<NX, CH>& sm = *reinterpret_cast<Smem<NX, CH>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
   const int64_t G = gridDim.x;
   const int64_t u0 = static_cast<int64_t>(blockIdx.x) * U / G;
   const int64_t u1 = (static_cast<int64_t>(blockIdx.x) + 1) * U / G;
   const int kbytes = K / 2;
-  const int KA = (K / 32 + 3) / 4;
+  const int KC = (kbytes + kRowBytes - 1) / kRowBytes;   // 128-byte chunks along K
+  const int KA = (K / 32 + 3) / 4;                       // scale atoms along K
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -396,13 +423,18 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           break;
         }
         const int64_t tile = u / KS;
-        const int ks = static_cast<int>(u % KS);
-        const int ka0 = 2 * ks;
-        const int na = min(2, KA - ka0);
+        const int c0 = static_cast<int>(u % KS) * CH;    // first 128-byte chunk
+        const int ka0 = 2 * c0;
+        const int na = min(2 * CH, KA - ka0);
         const uint32_t fb = smem_u32(&sm.full[s]);
-        mbar_arrive_expect_tx(fb, (128 + NX) * kRowBytes + 2 * na * kSfAtom);
-        tma_load_2d_hint(smem_u32(sm.w[s]), &tmW, fb, ks * kRowBytes, static_cast<int32_t>(tile * 128), stream);
-        tma_load_2d_hint(smem_u32(sm.x[s]), &tmX, fb, ks * kRowBytes, 0, keep);
+        mbar_arrive_expect_tx(fb, CH * (128 + NX) * kRowBytes + 2 * na * kSfAtom);
+        if (CH == 1) {
+          tma_load_2d_hint(smem_u32(sm.w[s]), &tmW, fb, c0 * kRowBytes, static_cast<int32_t>(tile * 128), stream);
+          tma_load_2d_hint(smem_u32(sm.x[s]), &tmX, fb, c0 * kRowBytes, 0, keep);
+        } else {
+          tma_load_3d_hint(smem_u32(sm.w[s]), &tmW, fb, 0, static_cast<int32_t>(tile * 128), c0, stream);
+          tma_load_3d_hint(smem_u32(sm.x[s]), &tmX, fb, 0, 0, c0, keep);
+        }
         bulk_load(smem_u32(sm.sfw[s]), sfW + (tile * KA + ka0) * kSfAtom, na * kSfAtom, fb);
         bulk_load(smem_u32(sm.sfx[s]), sfX + static_cast<int64_t>(ka0) * kSfAtom, na * kSfAtom, fb);
       }
@@ -420,7 +452,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const bool last = (u == u1 - 1) || ks == KS - 1;
         const uint32_t buf = seg & 1u;
         if (sm.abort_flag) break;
-        if (first && !mbar_wait(smem_u32(&sm.tempty[buf]), ((seg >> 1) & 1u) ^ 1u)) {
+        // completion k of tempty[buf] = the k-th time the epilogue handed the
+        // (zeroed) buffer back; completion 0 is the initial zeroing
+        if (first && !mbar_wait(smem_u32(&sm.tempty[buf]), (seg >> 1) & 1u)) {
           raise_abort(&sm.abort_flag);
           break;
         }
@@ -429,22 +463,29 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           break;
         }
         tc_fence_after();
-        const int ka0 = 2 * ks;
-        const int na = min(2, KA - ka0);
-        const uint32_t sfc = tmem + kSfBase + s * kSfColsPerStage;
+        const int c0 = ks * CH;
+        const int ka0 = 2 * c0;
+        const int na = min(2 * CH, KA - ka0);
+        const uint32_t sfc = tmem + kSfBase + s * kSfCols;
+        const uint32_t d = tmem + buf * kAccCols;
         for (int a = 0; a < na; ++a) {
-          tc_cp_32x128b_warpx4(sfc + 4 * a, sdesc_sf_32x16(smem_u32(sm.sfw[s] + a * kSfAtom)));
-          tc_cp_32x128b_warpx4(sfc + 8 + 4 * a, sdesc_sf_32x16(smem_u32(sm.sfx[s] + a * kSfAtom)));
+          tc_cp_32x128b_warpx4(sfc + 16 * (a >> 1) + 4 * (a & 1),
+                               sdesc_sf_32x16(smem_u32(sm.sfw[s] + a * kSfAtom)));
+          tc_cp_32x128b_warpx4(sfc + 16 * (a >> 1) + 8 + 4 * (a & 1),
+                               sdesc_sf_32x16(smem_u32(sm.sfx[s] + a * kSfAtom)));
         }
-        const uint64_t wd = sdesc_kmajor_sw128(smem_u32(sm.w[s]));
-        const uint64_t xd = sdesc_kmajor_sw128(smem_u32(sm.x[s]));
-        const int rem = kbytes - ks * kRowBytes;
-        const int nk = min(4, (rem + 31) / 32);
-        const uint32_t d = tmem + buf * 32;
-        for (int kk = 0; kk < nk; ++kk) {
-          const uint32_t id = idesc_mxf4(128, NX, (kk & 1) * 2, (kk & 1) * 2);
-          mma_mxf4(d, wd + 2 * kk, xd + 2 * kk, id, sfc + 4 * (kk >> 1), sfc + 8 + 4 * (kk >> 1),
-                   (!first || kk > 0) ? 1u : 0u);
+        const int nch = min(CH, KC - c0);
+        for (int j = 0; j < nch; ++j) {
+          const uint64_t wd = sdesc_kmajor_sw128(smem_u32(sm.w[s] + j * kSlab));
+          const uint64_t xd = sdesc_kmajor_sw128(smem_u32(sm.x[s] + j * NX * kRowBytes));
+          const int rem = kbytes - (c0 + j) * kRowBytes;
+          const int nk = min(4, (rem + 31) / 32);
+          const uint32_t sfj = sfc + 16 * j;
+          for (int kk = 0; kk < nk; ++kk) {
+            const uint32_t id = idesc_mxf4(128, NX, (kk & 1) * 2, (kk & 1) * 2);
+            mma_mxf4(d + (kk % kAcc) * NX, wd + 2 * kk, xd + 2 * kk, id, sfj + 4 * (kk >> 1),
+                     sfj + 8 + 4 * (kk >> 1), 1u);
+          }
         }
         tc_commit(smem_u32(&sm.empty[s]));
         if (last) {
@@ -459,6 +500,21 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   } else {
     // ---------------------------------------------------------- epilogue
     const int row = warp * 32 + lane;               // weight row within the tile
+    const uint32_t lane_taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    {
+      // zero both accumulator buffers and hand them to the MMA thread
+      uint32_t z[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) z[j] = 0u;
+      for (int c = 0; c < 2 * kAccCols; c += 16) tmem_st_16(lane_taddr + c, z);
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&sm.tempty[0]));
+        mbar_arrive(smem_u32(&sm.tempty[1]));
+      }
+    }
     uint32_t seg = 0;
     int64_t u = u0;
     while (u < u1) {
@@ -473,15 +529,24 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       tc_fence_after();
       float acc[NX];
       {
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + buf * 32;
+        const uint32_t taddr = lane_taddr + buf * kAccCols;
+        uint32_t z[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) z[j] = 0u;
 #pragma unroll
         for (int c = 0; c < NX / 16; ++c) {
-          uint32_t r[16];
-          tmem_ld_16(taddr + c * 16, r);
-          tc_wait_ld_16(r);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc[c * 16 + j] = __uint_as_float(r[j]);
+          for (int a = 0; a < kAcc; ++a) {
+            uint32_t r[16];
+            tmem_ld_16(taddr + a * NX + c * 16, r);
+            tc_wait_ld_16(r);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              acc[c * 16 + j] = (a == 0 ? 0.0f : acc[c * 16 + j]) + __uint_as_float(r[j]);
+            tmem_st_16(taddr + a * NX + c * 16, z);    // zero for the next segment
+          }
         }
+        tc_wait_st();
       }
       tc_fence_before();
       __syncwarp();
@@ -611,6 +676,30 @@ size_t gemm_mxfp4_decode_workspace(int M, int N, int K, int num_sms) {
   return floats * sizeof(float) + static_cast<size_t>(p.tiles) * sizeof(uint32_t);
 }
 
+namespace {
+template <int NX, int CH, bool BF>
+cudaError_t launch_decode_variant(const Mxfp4GemmArgs& a, const decode::Plan& p, float* ws,
+                                  uint32_t* counters, cudaStream_t s) {
+  using namespace decode;
+  CUtensorMap tmX, tmW;
+  const uint64_t kb = static_cast<uint64_t>(a.K) / 2;
+  if (CH == 1) {
+    if (!make_kmajor_map(&tmX, a.A, kb, a.M, kb, NX) || !make_kmajor_map(&tmW, a.B, kb, a.N, kb, 128))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!make_kmajor_map_chunked(&tmX, a.A, kb, a.M, kb, NX, CH) ||
+        !make_kmajor_map_chunked(&tmW, a.B, kb, a.N, kb, 128, CH))
+      return cudaErrorInvalidValue;
+  }
+  const size_t smem = sizeof(Smem<NX, CH>) + 1024;
+  cudaError_t e = set_smem(gemm_mxfp4_decode_kernel<NX, CH, BF>, smem);
+  if (e != cudaSuccess) return e;
+  gemm_mxfp4_decode_kernel<NX, CH, BF><<<static_cast<int>(p.G), kDecThreads, smem, s>>>(
+      tmX, tmW, a.sfA, a.sfB, a.C, a.D, a.M, a.N, a.K, p.KS, p.U, p.smax, ws, counters);
+  return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_gemm_mxfp4_decode(const Mxfp4GemmArgs& a, int num_sms, cudaStream_t s) {
   using namespace decode;
   const Plan p = make_plan(a.N, a.K, num_sms);
@@ -618,23 +707,17 @@ cudaError_t launch_gemm_mxfp4_decode(const Mxfp4GemmArgs& a, int num_sms, cudaSt
   float* ws = static_cast<float*>(a.workspace);
   uint32_t* counters =
       ws == nullptr ? nullptr : reinterpret_cast<uint32_t*>(ws + p.tiles * p.smax * nx * 128);
-  const int grid = static_cast<int>(p.G);
-  cudaError_t e;
-#define BSG_LAUNCH_DECODE(NXV, BF)                                                               \
-  do {                                                                                           \
-    const size_t smem = sizeof(Smem<NXV>) + 1024;                                                \
-    e = set_smem(gemm_mxfp4_decode_kernel<NXV, BF>, smem);                                       \
-    if (e != cudaSuccess) return e;                                                              \
-    gemm_mxfp4_decode_kernel<NXV, BF><<<grid, kDecThreads, smem, s>>>(                              \
-        a.tmA, a.tmB, a.sfA, a.sfB, a.C, a.D, a.M, a.N, a.K, p.KS, p.U, p.smax, ws, counters);   \
-  } while (0)
-  if (nx == 16) {
-    if (a.out_bf16) BSG_LAUNCH_DECODE(16, true); else BSG_LAUNCH_DECODE(16, false);
-  } else {
-    if (a.out_bf16) BSG_LAUNCH_DECODE(32, true); else BSG_LAUNCH_DECODE(32, false);
+  const int key = (nx == 16 ? 0 : 4) | (p.ch == 1 ? 0 : 2) | (a.out_bf16 ? 1 : 0);
+  switch (key) {
+    case 0: return launch_decode_variant<16, 1, false>(a, p, ws, counters, s);
+    case 1: return launch_decode_variant<16, 1, true>(a, p, ws, counters, s);
+    case 2: return launch_decode_variant<16, kChunksWide, false>(a, p, ws, counters, s);
+    case 3: return launch_decode_variant<16, kChunksWide, true>(a, p, ws, counters, s);
+    case 4: return launch_decode_variant<32, 1, false>(a, p, ws, counters, s);
+    case 5: return launch_decode_variant<32, 1, true>(a, p, ws, counters, s);
+    case 6: return launch_decode_variant<32, kChunksWide, false>(a, p, ws, counters, s);
+    default: return launch_decode_variant<32, kChunksWide, true>(a, p, ws, counters, s);
   }
-#undef BSG_LAUNCH_DECODE
-  return cudaGetLastError();
 }
 
 }  // namespace bsg

@@ -31,6 +31,18 @@ cudaError_t launch_quantize_mxfp4(const void* x, bool src_bf16, int64_t rows, in
 cudaError_t launch_sf_to_tcgen05(const uint8_t* sf, int64_t rows, int64_t kblocks, uint8_t* out,
                                  cudaStream_t s);
 
+// ------------------------------------------------------------- tensor maps
+// 2-D map of a byte matrix (rows x inner_bytes, row pitch `pitch`) loaded in
+// boxes of box_rows x 128 bytes with 128-byte swizzling; out of range = 0.
+bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
+                     uint64_t pitch, uint32_t box_rows);
+// 3-D view [chunk][row][128 B] of the same matrix (inner_bytes % 128 == 0):
+// one box brings box_chunks consecutive 128-byte chunks of box_rows rows and
+// lands as box_chunks canonical (box_rows x 128 B, swizzled) slabs.
+bool make_kmajor_map_chunked(CUtensorMap* map, const void* base, uint64_t inner_bytes,
+                             uint64_t rows, uint64_t pitch, uint32_t box_rows,
+                             uint32_t box_chunks);
+
 // ----------------------------------------------------------------- GEMMs
 struct Fp8GemmArgs {
   int M, N, K;
@@ -53,7 +65,10 @@ struct Mxfp4GemmArgs {
   const float* C;
   void* D;
   bool out_bf16;
-  CUtensorMap tmA, tmB;      // packed operands (box 128 B x rows)
+  CUtensorMap tmA, tmB;      // packed operands (box 128 B x rows); the decode
+                             // launcher encodes its own maps from A and B
+  const void* A;
+  const void* B;
   void* workspace;           // split-K partials + tile counters (decode path)
   size_t workspace_bytes;
 };
