@@ -15,10 +15,12 @@ Workloads (synthetic, seeded; see synth/):
               bytes (weights + scales + activations + output).
   fp8_256, mxfp4_1024   the small parity configurations (latency-bound).
 
-One JSON line is printed by rank 0.  Timing: W warm-up steps, then K steps, each
-bracketed by CUDA events on the launching stream, with an L2 flush (a 256 MB
-write) before every timed step, outside the events.  The GEMM kernel is also
-timed alone per step (roofline).  `e2e` repeats the step through the same API
+One JSON line is printed by rank 0.  Timing: W warm-up steps, then K steps.
+The step (quantise + GEMM) is captured once as a CUDA graph; each timed step
+is one replay bracketed by CUDA events on the launching stream, with an L2
+flush before it, outside the events (a 256 MB write, then a 256 MB read so
+no dirty lines are left to evict inside the timed step).  The GEMM alone is
+captured and timed the same way for K more replays (roofline).  `e2e` repeats the step through the same API
 with the activations copied from pinned host memory and the output copied back
 inside the timed region.  `cpu_baseline` times the CPU oracle on a bounded
 sample of the same workload.  Under torchrun every rank runs an independent
@@ -47,6 +49,32 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # nominal dense ratios to BF16 (2.25 PF): FP8 4.5 PF, FP4 13.5 PF
 RATIO = {"fp8": 2.0, "fp4": 6.0}
 L2_FLUSH_BYTES = 256 << 20
+
+
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = {"fp8": ["gemm_fp8.cu", "common.cuh"], "fp4": ["gemm_mxfp4.cu", "common.cuh"]}
+
+
+def kernel_source_hash(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "fp4_gemm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload, kind):
+    """DRAM bytes per launch of the workload's GEMM from the committed ncu
+    summary, or None when there is none or the kernel source changed since."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            entry = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not entry or entry.get("src_sha") != kernel_source_hash(KERNEL_SOURCES[kind]):
+        return None
+    return entry.get("dram_bytes")
 
 
 def peaks():
@@ -322,6 +350,14 @@ def main():
     bsg.load_library()
     w = Workload(args.workload, args.m, dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    clean = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2(i):
+        # write a buffer larger than L2, then read another one, so the timed
+        # step starts with none of its data in L2 and no dirty lines to evict
+        flush.fill_(float(i))
+        clean.sum()
+
     stream = torch.cuda.current_stream()
 
     for _ in range(max(args.warmup, 0)):
@@ -330,8 +366,27 @@ def main():
     if bsg.bsg_device_error() != 0:
         raise RuntimeError("device error during warm-up")
 
+    # The step (quantise + GEMM) and the GEMM alone are captured once as CUDA
+    # graphs and replayed, so the device time excludes host launch gaps.
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        return g
+
+    g_step = capture(w.step)
+    g_gemm = capture(w.gemm)
+    for _ in range(2):
+        g_step.replay()
+        g_gemm.replay()
+    torch.cuda.synchronize()
+
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     clocks = Clocks(local)
     if dist is not None:
         dist.barrier()
@@ -339,20 +394,23 @@ def main():
     clocks.start()
     t_wall0 = time.perf_counter()
     for i in range(K):
-        flush.fill_(float(i))                       # L2 flush, outside the events
+        flush_l2(i)                                 # outside the events
         ev[i][0].record(stream)
-        w.quantize()
+        g_step.replay()
         ev[i][1].record(stream)
-        w.gemm()
+    for i in range(K):
+        flush_l2(i)
         ev[i][2].record(stream)
+        g_gemm.replay()
+        ev[i][3].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall0
     clk = clocks.stop()
     if bsg.bsg_device_error() != 0:
         raise RuntimeError("device error during the timed steps")
-    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
-    gemm_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    quant_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    gemm_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
+    quant_ms = [max(a - b, 0.0) for a, b in zip(step_ms, gemm_ms)]
     ms = statistics.mean(step_ms)
     if dist is not None:
         t = torch.tensor([ms], device=dev)
@@ -392,7 +450,7 @@ def main():
         achieved = w.gemm_bytes() / g_s / 1e9
         peak = pk["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak, "traffic": measured_traffic(w.name, "fp4"),
                 "kernel": "gemm_mxfp4_decode_kernel",
                 "peak_source": f"{pk_kind} HBM copy bandwidth"}
     else:
@@ -400,7 +458,7 @@ def main():
         achieved = w.flops() / g_s / 1e12
         peak = pk["bf16_tflops"] * RATIO[dt]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak, "traffic": measured_traffic(w.name, dt),
                 "kernel": "gemm_mxfp4_kernel" if w.fp4 else "gemm_fp8_kernel",
                 "peak_source": f"{pk_kind} cuBLAS BF16 burst x {RATIO[dt]:g} (nominal dense "
                                f"{dt.upper()}:BF16 ratio)"}
@@ -414,12 +472,14 @@ def main():
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
                    "a": f"{w.fa}/{w.ga}", "b": f"{w.fb}/{w.gb}", "out": w.out,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "flushed (256 MB write) before every timed step"},
+                   "l2": "flushed before every timed step (256 MB write, then a 256 MB read)",
+                   "timing": "CUDA events around a CUDA-graph replay of each step"},
         "quantize_ms": statistics.mean(quant_ms), "gemm_ms": statistics.mean(gemm_ms),
+        "gemm_ms_min": min(gemm_ms),
         "wall_s": wall,
         "roofline": roof,
         "clocks": clk,
-        "gpu_launches": w.launches_per_step * K,
+        "gpu_launches": (w.launches_per_step + 1) * K,   # step replays + GEMM-only replays
     }
     if e2e is not None:
         line["e2e"] = e2e
