@@ -227,7 +227,9 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
     a.C = C;
     a.D = D;
     a.out_bf16 = out == BSG_BF16;
-    if (!make_kmajor_map(&a.tmA, A, K, M, K, 128) || !make_kmajor_map(&a.tmB, B, K, N, K, 256))
+    a.pair = bsg::gemm_fp8_use_pair(a.M, a.N, sms);
+    if (!make_kmajor_map(&a.tmA, A, K, M, K, 128) ||
+        !make_kmajor_map(&a.tmB, B, K, N, K, static_cast<uint32_t>(bsg::gemm_fp8_b_box_rows(a.pair))))
       return BSG_ERR_CUDA;
     return from_cuda(bsg::launch_gemm_fp8(a, sms, s));
   }

@@ -15,20 +15,30 @@
 // lives in tensor memory, double-buffered, so the MMA of tile t+1 overlaps
 // the drain of tile t.
 //
-// Warp roles (384 threads = 3 warpgroups, one CTA per SM, persistent over
-// output tiles):
-//   warp 0     producer: TMA loads of A (128 x 128 B) and B (256 x 128 B)
-//              into a 4-stage ring; cp.async of the K tile's scales into an
-//              8-slot scale ring.
-//   warp 1     tensor-memory allocator and MMA issuer (one lane).
+// Two shapes of the same kernel:
+//   * single CTA: 128 x 256 output tiles; per K tile the SM loads A 16 KB +
+//     B 32 KB into a 4-stage ring;
+//   * CTA pair (a cluster of two on neighbouring SMs, tcgen05 cta_group::2):
+//     256 x 256 tiles.  Each CTA loads its 128 rows of A and 128 of the 256
+//     rows of B (32 KB per K tile, 6 stages); one thread of the even CTA
+//     issues M = 256 MMAs that read both CTAs' shared memory and write each
+//     CTA's 128 rows of the partial into its own tensor memory.  Per FLOP an
+//     SM moves two thirds of the single-CTA bytes and keeps more K tiles in
+//     flight.
+//
+// Warp roles (384 threads = 3 warpgroups, one CTA per SM, persistent):
+//   warp 0     producer: TMA loads of A and B; cp.async of the K tile's
+//              scales into an 8-slot ring.
+//   warp 1     tensor-memory allocator; MMA issuer (one lane; in a pair only
+//              the even CTA's).
 //   warps 2-3  idle (they complete warpgroup 0).
 //   warps 4-11 promotion + epilogue: warpgroups 1 and 2.  Warp w reads TMEM
 //              lanes 32*(w%4)..+31 (its rows) and column half (w-4)/4 of the
 //              256-wide tile.
 // Registers: the kernel launches at 168 per thread (384 x 168 = 64512);
-// warpgroup 0 gives back down to 40 and the promotion warpgroups take 232
-// each, 128 x 40 + 256 x 232 = 64512, which holds 128 FP32 accumulators plus
-// two 32-column TMEM load buffers per thread without spilling.  The drain
+// warpgroup 0 gives back down to 56 and the promotion warpgroups take 224
+// each, 128 x 56 + 256 x 224 = 64512, which holds 128 FP32 accumulators plus
+// two 16-column TMEM load buffers per thread without spilling.  The drain
 // uses paired FP32 FMAs (fma.rn.f32x2), one instruction per two elements.
 // Every wait is bounded; a wait that runs out sets the error word, raises a
 // CTA-wide abort flag and all roles unwind to the final barrier.
@@ -40,10 +50,9 @@ namespace {
 
 __device__ uint32_t g_fp8_error = 0;
 
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BM = 128;            // output rows per CTA
+constexpr int BN = 256;            // output columns per tile
 constexpr int BK = 128;            // one scale tile along K = one promotion unit
-constexpr int kStages = 4;
 constexpr int kScaleSlots = 8;
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 0;
@@ -54,16 +63,27 @@ constexpr int kRegsLarge = 224;    // promotion warpgroups after setmaxnreg.inc
 static_assert(128 * kRegsSmall + 256 * kRegsLarge <= kThreads * 168,
               "register split exceeds the launch allocation");
 constexpr int kTmemCols = 512;     // two 256-column FP32 partial buffers
-constexpr int kGroupM = 8;         // tile raster: groups of 8 M tiles
+constexpr int kGroup = 8;          // tile raster: groups of 8 tiles
 
+template <bool kPair>
+struct Cfg {
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kBRows = kPair ? BN / 2 : BN;        // B rows this CTA loads
+  static constexpr int kTileM = kPair ? 2 * BM : BM;        // rows of a tile
+  static constexpr int kPromoArrivals = kPair ? 16 : 8;     // drains per TMEM buffer
+  static constexpr uint32_t kStageBytes = (BM + kBRows) * BK;
+  static constexpr uint32_t kFullBytes = (kPair ? 2 : 1) * kStageBytes;
+};
+
+template <bool kPair>
 struct __align__(1024) Smem {
-  uint8_t a[kStages][BM * BK];
-  uint8_t b[kStages][BN * BK];
+  uint8_t a[Cfg<kPair>::kStages][BM * BK];
+  uint8_t b[Cfg<kPair>::kStages][Cfg<kPair>::kBRows * BK];
   float sa[kScaleSlots][BM];
   float sb[kScaleSlots][BN];
   uint8_t epi[8][32 * 64];   // per promotion warp: 32 rows x 64 B output staging
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[Cfg<kPair>::kStages];
+  uint64_t empty[Cfg<kPair>::kStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t sfull[kScaleSlots];
@@ -77,40 +97,45 @@ struct TileCoord {
   int m, n;
 };
 
-// Raster of the persistent tile loop.  Tiles are visited in groups of
-// kGroupM rows of tiles along one dimension while the other is swept, so the
-// operand panel of the group stays in L2 and the swept operand is re-read
-// from L2.  along_n = true groups along N (sweeps M): chosen when A is the
-// smaller operand, so the whole of A is what gets re-read and stays resident.
+// Raster of the persistent tile loop.  Tiles are visited in groups of kGroup
+// rows of tiles along one dimension while the other is swept, so the operand
+// panel of the group stays in L2 and the swept operand is re-read from L2.
+// along_n = true groups along N (sweeps M): chosen when A is the smaller
+// operand, so the whole of A is what gets re-read and stays resident.
 __device__ __forceinline__ TileCoord tile_coord(int t, int num_m, int num_n, bool along_n) {
   const int outer = along_n ? num_n : num_m;
   const int inner = along_n ? num_m : num_n;
-  const int group_size = kGroupM * inner;
+  const int group_size = kGroup * inner;
   const int group = t / group_size;
-  const int first = group * kGroupM;
-  const int gsz = min(outer - first, kGroupM);
+  const int first = group * kGroup;
+  const int gsz = min(outer - first, kGroup);
   const int local = t % group_size;
   const int o = first + local % gsz, i = local / gsz;
   return along_n ? TileCoord{i, o} : TileCoord{o, i};
 }
 
-__device__ __forceinline__ void raise_abort(Smem& sm) {
+__device__ __forceinline__ void raise_abort(volatile uint32_t* flag) {
   atomicOr(&g_fp8_error, kErrTimeout);
-  sm.abort_flag = 1u;
+  *flag = 1u;
 }
 
-template <bool kARow, bool kBRow, bool kBF16Out>
+template <bool kPair, bool kARow, bool kBRow, bool kBF16Out>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const float* __restrict__ sA, const float* __restrict__ sB,
                     const float* __restrict__ Cin, void* __restrict__ Dout, int M, int N, int K,
                     uint32_t idesc, bool vec_out, bool raster_n) {
+  using C = Cfg<kPair>;
+  constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                      ~static_cast<uintptr_t>(1023));
+  Smem<kPair>& sm = *reinterpret_cast<Smem<kPair>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
-  const int num_m = (M + BM - 1) / BM;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;      // 0 = the pair's MMA issuer
+  const int unit = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int units = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int num_m = (M + C::kTileM - 1) / C::kTileM;
   const int num_n = (N + BN - 1) / BN;
   const int tiles = num_m * num_n;
   const int KT = (K + BK - 1) / BK;
@@ -123,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&sm.tfull[b]), 1);
-      mbar_init(smem_u32(&sm.tempty[b]), 8);
+      mbar_init(smem_u32(&sm.tempty[b]), C::kPromoArrivals);
     }
     for (int s = 0; s < kScaleSlots; ++s) {
       mbar_init(smem_u32(&sm.sfull[s]), 32);
@@ -134,8 +159,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
-    tmem_relinquish();
+    if (kPair) {
+      tmem_alloc_pair(smem_u32(&sm.tmem_base), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+      tmem_relinquish();
+    }
   }
   if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmA);
@@ -143,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (kPair) cluster_sync();    // barriers and tensor memory of both CTAs are ready
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
@@ -152,8 +183,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t keep = l2_policy_evict_last();   // operands are re-read by other tiles
     uint32_t it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+    for (int t = unit; t < tiles && ok; t += units) {
       const TileCoord tc = tile_coord(t, num_m, num_n, raster_n);
+      const int m_cta = tc.m * C::kTileM + static_cast<int>(rank) * BM;   // this CTA's rows
+      const int n_b = tc.n * BN + static_cast<int>(rank) * (BN - C::kBRows);   // its B rows
       for (int kt = 0; kt < KT; ++kt, ++it) {
         if (sm.abort_flag) { ok = false; break; }
         const int s = static_cast<int>(it % kStages);
@@ -166,24 +199,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                  mbar_wait(smem_u32(&sm.sempty[ss]), phs ^ 1u);
           if (good) {
             const uint32_t fb = smem_u32(&sm.full[s]);
-            mbar_arrive_expect_tx(fb, (BM + BN) * BK);
-            tma_load_2d_hint(smem_u32(sm.a[s]), &tmA, fb, kt * BK, tc.m * BM, keep);
-            tma_load_2d_hint(smem_u32(sm.b[s]), &tmB, fb, kt * BK, tc.n * BN, keep);
+            if (kPair) {
+              // both CTAs' loads complete on the even CTA's barrier
+              if (rank == 0) mbar_arrive_expect_tx(fb, C::kFullBytes);
+              const uint32_t fb0 = mapa_shared(fb, 0);
+              tma_load_2d_pair(smem_u32(sm.a[s]), &tmA, fb0, kt * BK, m_cta, keep);
+              tma_load_2d_pair(smem_u32(sm.b[s]), &tmB, fb0, kt * BK, n_b, keep);
+            } else {
+              mbar_arrive_expect_tx(fb, C::kFullBytes);
+              tma_load_2d_hint(smem_u32(sm.a[s]), &tmA, fb, kt * BK, m_cta, keep);
+              tma_load_2d_hint(smem_u32(sm.b[s]), &tmB, fb, kt * BK, n_b, keep);
+            }
           } else {
-            raise_abort(sm);
+            raise_abort(&sm.abort_flag);
           }
         }
         good = __shfl_sync(0xffffffffu, good, 0);
         if (!good) { ok = false; break; }
-        // scales of this K tile -> scale slot ss
+        // scales of this K tile -> scale slot ss (this CTA's rows, all 256 columns)
         if (kARow) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const int r = tc.m * BM + 4 * lane + j;
+            const int r = m_cta + 4 * lane + j;
             if (r < M) cp_async_4(smem_u32(&sm.sa[ss][4 * lane + j]), sA + static_cast<int64_t>(kt) * M + r);
           }
         } else if (lane == 0) {
-          cp_async_4(smem_u32(&sm.sa[ss][0]), sA + static_cast<int64_t>(tc.m) * KT + kt);
+          cp_async_4(smem_u32(&sm.sa[ss][0]), sA + static_cast<int64_t>(m_cta / BM) * KT + kt);
         }
         if (kBRow) {
 #pragma unroll
@@ -200,15 +241,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     cp_async_wait_all();
-    if (lane == 0) drain_fills(sm.full, kStages, it);
+    // the even CTA's full barriers also count the peer's bytes
+    if (lane == 0 && rank == 0) drain_fills(sm.full, kStages, it);
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
     setmaxnreg_dec<kRegsSmall>();
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      for (int t = unit; t < tiles && ok; t += units) {
         for (int kt = 0; kt < KT; ++kt, ++it) {
           if (sm.abort_flag) { ok = false; break; }
           const uint32_t b = it & 1u;
@@ -217,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ph = (it / kStages) & 1u;
           if (!mbar_wait(smem_u32(&sm.tempty[b]), tph ^ 1u) ||
               !mbar_wait(smem_u32(&sm.full[s]), ph)) {
-            raise_abort(sm);
+            raise_abort(&sm.abort_flag);
             ok = false;
             break;
           }
@@ -226,15 +268,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sm.b[s]));
           const uint32_t d = tmem + b * BN;
 #pragma unroll
-          for (int kk = 0; kk < BK / 32; ++kk)
-            mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : 0u);
-          tc_commit(smem_u32(&sm.empty[s]));
-          tc_commit(smem_u32(&sm.tfull[b]));
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            if (kPair)
+              mma_f8f6f4_pair(d, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+            else
+              mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+          }
+          if (kPair) {
+            tc_commit_pair_mc(smem_u32(&sm.empty[s]), 3);
+            tc_commit_pair_mc(smem_u32(&sm.tfull[b]), 3);
+          } else {
+            tc_commit(smem_u32(&sm.empty[s]));
+            tc_commit(smem_u32(&sm.tfull[b]));
+          }
         }
       }
       // every MMA this thread issued has completed once final_bar flips
-      tc_commit(smem_u32(&sm.final_bar));
-      if (!mbar_wait(smem_u32(&sm.final_bar), 0)) raise_abort(sm);
+      if (kPair)
+        tc_commit_pair(smem_u32(&sm.final_bar));
+      else
+        tc_commit(smem_u32(&sm.final_bar));
+      if (!mbar_wait(smem_u32(&sm.final_bar), 0)) raise_abort(&sm.abort_flag);
     }
     __syncwarp();
   } else if (warp < kFirstPromoWarp) {
@@ -247,9 +301,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = q * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + g * 128;
     const uint64_t stream_out = l2_policy_evict_first();   // the result is not re-read
+    // where this warp reports a drained buffer: the issuing CTA's barrier
+    const uint32_t tempty0 = kPair ? mapa_shared(smem_u32(&sm.tempty[0]), 0) : smem_u32(&sm.tempty[0]);
     uint32_t it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+    for (int t = unit; t < tiles && ok; t += units) {
       const TileCoord tc = tile_coord(t, num_m, num_n, raster_n);
       uint64_t acc[64];                            // 128 FP32 accumulators, in pairs
 #pragma unroll
@@ -261,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t phs = (it / kScaleSlots) & 1u;
         if (sm.abort_flag || !mbar_wait(smem_u32(&sm.sfull[ss]), phs) ||
             !mbar_wait(smem_u32(&sm.tfull[b]), tph)) {
-          if (!sm.abort_flag) raise_abort(sm);
+          if (!sm.abort_flag) raise_abort(&sm.abort_flag);
           ok = false;
           break;
         }
@@ -293,8 +349,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(smem_u32(&sm.tempty[b]));
-          mbar_arrive(smem_u32(&sm.sempty[ss]));
+          // this warp's reads of the buffer and of the scale slot are complete
+          // (wait::ld returned, the scales were used): nothing to publish
+          mbar_arrive_relaxed(tempty0 + b * 8);
+          mbar_arrive_relaxed(smem_u32(&sm.sempty[ss]));
         }
       }
       if (!ok) break;
@@ -303,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // pieces XOR-swizzled by row, so both phases are bank-conflict free)
       // and writes back 8 rows x 64 contiguous bytes per store instruction
       // instead of 32 scattered 16-byte pieces.
-      const int64_t row0 = static_cast<int64_t>(tc.m) * BM + q * 32;
+      const int64_t row0 = static_cast<int64_t>(tc.m) * C::kTileM + rank * BM + q * 32;
       const int gcol0 = tc.n * BN + g * 128;
       const uint32_t stage = smem_u32(sm.epi[warp - kFirstPromoWarp]);
       constexpr int kElem = kBF16Out ? 2 : 4;
@@ -371,29 +429,79 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (kPair) cluster_sync();    // neither CTA leaves while the other may still signal it
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if (kPair)
+      tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      tmem_dealloc(tmem, kTmemCols);
+  }
+  if (kPair) {
+    __syncthreads();
+    cluster_sync();
   }
 }
 
-template <bool kARow, bool kBRow, bool kBF16Out>
+template <bool kPair, bool kARow, bool kBRow, bool kBF16Out>
 cudaError_t launch_variant(const Fp8GemmArgs& a, int num_sms, cudaStream_t s) {
-  auto kern = gemm_fp8_kernel<kARow, kBRow, kBF16Out>;
-  const size_t smem = sizeof(Smem) + 1024;
+  auto kern = gemm_fp8_kernel<kPair, kARow, kBRow, kBF16Out>;
+  const size_t smem = sizeof(Smem<kPair>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  const uint32_t idesc = idesc_f8f6f4(static_cast<uint32_t>(a.afmt), static_cast<uint32_t>(a.bfmt), BM, BN);
+  const int tile_m = Cfg<kPair>::kTileM;
+  const int tiles = ((a.M + tile_m - 1) / tile_m) * ((a.N + BN - 1) / BN);
+  const int per = kPair ? 2 : 1;
+  int max_units = num_sms / per;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = per;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (kPair) {
+    // A pair needs two SMs of one GPC; not every SM may find a partner, so a
+    // persistent grid is sized by how many pairs can be resident at once.
+    static int resident_pairs = 0;
+    if (resident_pairs == 0) {
+      cfg.gridDim = dim3(static_cast<unsigned>(2 * max_units));
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) resident_pairs = n;
+      else resident_pairs = max_units;
+    }
+    if (resident_pairs < max_units) max_units = resident_pairs;
+  }
+  const int grid = per * (tiles < max_units ? tiles : max_units);
+  const uint32_t idesc = idesc_f8f6f4(static_cast<uint32_t>(a.afmt), static_cast<uint32_t>(a.bfmt),
+                                      tile_m, BN);
   const bool vec_out = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) &&
                        (a.out_bf16 ? (a.N % 8 == 0) : (a.N % 4 == 0));
   // keep the smaller operand resident: sweep it inside groups of the larger
   const bool raster_n = static_cast<int64_t>(a.M) < static_cast<int64_t>(a.N);
-  kern<<<grid, kThreads, smem, s>>>(a.tmA, a.tmB, a.sA, a.sB, a.C, a.D, a.M, a.N, a.K, idesc,
-                                    vec_out, raster_n);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.sA, a.sB, a.C, a.D, a.M, a.N, a.K, idesc,
+                            vec_out, raster_n);
+}
+
+template <bool kPair>
+cudaError_t launch_shape(const Fp8GemmArgs& a, int num_sms, cudaStream_t s) {
+  const int key = (a.a_row ? 4 : 0) | (a.b_row ? 2 : 0) | (a.out_bf16 ? 1 : 0);
+  switch (key) {
+    case 0: return launch_variant<kPair, false, false, false>(a, num_sms, s);
+    case 1: return launch_variant<kPair, false, false, true>(a, num_sms, s);
+    case 2: return launch_variant<kPair, false, true, false>(a, num_sms, s);
+    case 3: return launch_variant<kPair, false, true, true>(a, num_sms, s);
+    case 4: return launch_variant<kPair, true, false, false>(a, num_sms, s);
+    case 5: return launch_variant<kPair, true, false, true>(a, num_sms, s);
+    case 6: return launch_variant<kPair, true, true, false>(a, num_sms, s);
+    default: return launch_variant<kPair, true, true, true>(a, num_sms, s);
+  }
 }
 
 }  // namespace
@@ -408,18 +516,19 @@ cudaError_t gemm_fp8_error_read_and_clear(cudaStream_t s, uint32_t* out) {
   return cudaStreamSynchronize(s);
 }
 
+int gemm_fp8_b_box_rows(bool pair) { return pair ? Cfg<true>::kBRows : Cfg<false>::kBRows; }
+
+bool gemm_fp8_use_pair(int M, int N, int num_sms) {
+  // Pairs need an even SM count and enough 256 x 256 tiles to fill the GPU.
+  // Measured on the two large FP8 workloads the two shapes are within a few
+  // per cent of each other; the pair is taken for M >= N (it splits B, the
+  // smaller operand then, between the two CTAs), the single CTA otherwise.
+  const int64_t pair_tiles = (static_cast<int64_t>(M) + 255) / 256 * ((N + BN - 1) / BN);
+  return num_sms >= 2 && M >= N && pair_tiles >= num_sms / 2;
+}
+
 cudaError_t launch_gemm_fp8(const Fp8GemmArgs& a, int num_sms, cudaStream_t s) {
-  const int key = (a.a_row ? 4 : 0) | (a.b_row ? 2 : 0) | (a.out_bf16 ? 1 : 0);
-  switch (key) {
-    case 0: return launch_variant<false, false, false>(a, num_sms, s);
-    case 1: return launch_variant<false, false, true>(a, num_sms, s);
-    case 2: return launch_variant<false, true, false>(a, num_sms, s);
-    case 3: return launch_variant<false, true, true>(a, num_sms, s);
-    case 4: return launch_variant<true, false, false>(a, num_sms, s);
-    case 5: return launch_variant<true, false, true>(a, num_sms, s);
-    case 6: return launch_variant<true, true, false>(a, num_sms, s);
-    default: return launch_variant<true, true, true>(a, num_sms, s);
-  }
+  return a.pair ? launch_shape<true>(a, num_sms, s) : launch_shape<false>(a, num_sms, s);
 }
 
 }  // namespace bsg

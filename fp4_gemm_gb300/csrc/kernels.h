@@ -54,8 +54,12 @@ struct Fp8GemmArgs {
   const float* C;            // optional FP32 addend
   void* D;
   bool out_bf16;
+  bool pair;                 // CTA-pair kernel (256 x 256 tiles, tcgen05 cta_group::2)
   CUtensorMap tmA, tmB;      // K-major operand maps (box 128 B x rows)
 };
+// Whether a problem takes the CTA-pair kernel, and the B box height it needs.
+bool gemm_fp8_use_pair(int M, int N, int num_sms);
+int gemm_fp8_b_box_rows(bool pair);
 cudaError_t launch_gemm_fp8(const Fp8GemmArgs& a, int num_sms, cudaStream_t s);
 
 struct Mxfp4GemmArgs {

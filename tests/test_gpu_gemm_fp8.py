@@ -60,3 +60,20 @@ def test_fp8_many_tiles_persistent():
     A, B = synth.make("ffn_up", m=2048, n=4096, k=256)
     rows = np.r_[0:3, 1000:1003, 2045:2048]
     report("persistent", *_run(A, B, "e4m3", "e4m3", "row", "tile", "bf16", rows=rows))
+
+
+def test_fp8_pair_path_ragged_bf16_addend():
+    # enough 256 x 256 tiles for the CTA-pair kernel; M, N ragged (odd number
+    # of 128-row blocks), rows sampled across both CTAs of a pair and the edges
+    M, N, K = 4100, 2000, 384
+    A, B = synth.make("ffn_up", m=M, n=N, k=K)
+    C = synth.addend("ffn_up", M, N)
+    rows = np.array([0, 1, 127, 128, 255, 256, 1000, 2047, 2048, 4095, 4096, 4099])
+    report("pair ragged", *_run(A, B, "e4m3", "e4m3", "row", "tile", "bf16", C=C, rows=rows))
+
+
+def test_fp8_pair_path_e5m2_fp32():
+    M, N, K = 2560, 2048, 1024
+    A, B = synth.make("dgrad", m=M, n=N, k=K)
+    rows = np.r_[0:4, 126:130, 254:258, 2556:2560]
+    report("pair e5m2", *_run(A, B, "e5m2", "e4m3", "tile", "tile", "f32", rows=rows))
