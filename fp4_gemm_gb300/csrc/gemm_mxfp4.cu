@@ -11,11 +11,13 @@
 // promotion step is needed because the scales are powers of two.
 //
 // Scale factors arrive in the BSG_SF_TCGEN05 atom layout (512 bytes per
-// 128 rows x 4 K-blocks), are bulk-copied to shared memory with the operands
-// and moved to tensor memory with tcgen05.cp.32x128b.warpx4 right before the
-// MMAs that use them (copy and MMA issued by one thread execute in order).
-// Each pipeline stage owns its own tensor-memory scale columns, so a copy
-// never overwrites scales an in-flight MMA still reads.
+// 128 rows x 4 K-blocks).  Each pipeline stage owns its own tensor-memory
+// scale columns, so new scales never overwrite ones an in-flight MMA still
+// reads.  The general kernel bulk-copies them to shared memory with the
+// operands and moves them to tensor memory with tcgen05.cp.32x128b.warpx4
+// right before the MMAs that use them (copy and MMA issued by one thread
+// execute in order).  The decode kernel, whose MMAs are too small to hide a
+// copy, has four warps store them with tcgen05.st instead.
 //
 // Two kernels:
 //  * gemm_mxfp4_kernel: 128 x 128 output tiles, persistent, warp-specialised
@@ -289,29 +291,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------- decode path
 namespace decode {
 
-constexpr int kDecThreads = 192;   // warps 0-3 epilogue, 4 producer, 5 MMA
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kTmemCols = 512;
+// Warp roles: 0-3 epilogue (tensor-memory lane quarters 0-3), 4-7 scale
+// writers (lane quarters 0-3), 8 TMA producer, 9 MMA issuer.
+constexpr int kDecThreads = 320;
+constexpr int kSfWarp0 = 4;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr int kSlab = 128 * kRowBytes;   // one 128-row x 128-byte weight slab
-// Each MMA is tiny (M128 x N<=32 x K64); consecutive MMAs rotate over kAcc
-// independent accumulators so they do not form one dependent chain.  The
-// epilogue sums them.
-constexpr int kAcc = 4;
-// K chunks of 128 bytes (256 FP4 values) per pipeline stage when K allows the
-// chunked 3-D tensor map (K % 256 == 0): each TMA call then reads CH * 128
-// contiguous bytes of every weight row instead of 128.
-constexpr int kChunksWide = 2;
+
+// K chunks of 128 bytes (256 FP4 values) per pipeline stage.  With the
+// chunked 3-D tensor map (K % 256 == 0) one TMA call reads CH * 128
+// contiguous bytes of every weight row.  Big stages matter here: every stage
+// costs the MMA thread one barrier wait, one fence and one commit (a few
+// hundred ns), while each of its M128 x N16 x K64 MMAs takes ~30 ns.
+__host__ __device__ constexpr int pow2_at_least(int v, int p) { return p >= v ? p : pow2_at_least(v, 2 * p); }
 
 template <int NX, int CH>
 struct Cfg {
-  static constexpr int kStageBytes = CH * (kSlab + NX * kRowBytes + 4 * kSfAtom);
-  static constexpr int kStages0 = (200 * 1024) / kStageBytes;
-  static constexpr int kStages = kStages0 > 10 ? 10 : kStages0;
+  static constexpr int kStageBytes = CH * (kSlab + NX * kRowBytes);
+  static constexpr int kStages0 = (216 * 1024) / kStageBytes;
+  static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
   static constexpr int kSfColsPerStage = CH * 16;   // per chunk: SFW 2 atoms + SFX 2 atoms
-  static constexpr int kAccCols = kAcc * NX;         // one buffer of accumulators
-  static constexpr int kSfBase = 2 * kAccCols;       // after the two buffers
-  static_assert(kSfBase + kStages * kSfColsPerStage <= kTmemCols, "TMEM columns");
+  static constexpr int kSfBase = 2 * NX;            // after the two accumulator buffers
+  static constexpr int kTmemCols = pow2_at_least(kSfBase + kStages * kSfColsPerStage, 32);
+  static_assert(kStages >= 2, "at least two stages");
+  static_assert(kTmemCols <= 512, "TMEM columns");
 };
 
 template <int NX, int CH>
@@ -319,14 +323,15 @@ struct __align__(1024) Smem {
   static constexpr int S = Cfg<NX, CH>::kStages;
   uint8_t w[S][CH * kSlab];
   uint8_t x[S][CH * NX * kRowBytes];
-  uint8_t sfw[S][CH * 2 * kSfAtom];
-  uint8_t sfx[S][CH * 2 * kSfAtom];
+  // TMA bytes of the stage landed and the four scale-writer warps stored its
+  // scales (so the MMA thread waits on one barrier per stage)
   uint64_t full[S];
-  uint64_t empty[S];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t empty[S];     // MMAs of the stage done: smem and scale columns free
+  uint64_t tfull[2];     // accumulator buffer holds a finished segment
+  uint64_t tempty[2];    // epilogue drained the buffer
   uint64_t final_bar;
   uint32_t tmem_base;
+  uint32_t fast_flag;
   uint32_t last_flag;
   volatile uint32_t abort_flag;
 };
@@ -339,14 +344,18 @@ __host__ __device__ __forceinline__ int64_t owner(int64_t u, int64_t U, int64_t 
 
 struct Plan {
   int64_t tiles, KS, U, G, smax;
-  int ch;
+  int nx, ch;
 };
 
-int chunks_for(int K) { return (K % 256 == 0) ? kChunksWide : 1; }
+int chunks_for(int K, int nx) {
+  if (K % 256 != 0) return 1;
+  return nx == 16 ? 4 : 2;
+}
 
-Plan make_plan(int N, int K, int num_sms) {
+Plan make_plan(int M, int N, int K, int num_sms) {
   Plan p;
-  p.ch = chunks_for(K);
+  p.nx = M <= 16 ? 16 : 32;
+  p.ch = chunks_for(K, p.nx);
   p.tiles = (N + 127) / 128;
   p.KS = (static_cast<int64_t>(K) / 2 + kRowBytes * p.ch - 1) / (kRowBytes * p.ch);
   p.U = p.tiles * p.KS;
@@ -359,6 +368,29 @@ Plan make_plan(int N, int K, int num_sms) {
   return p;
 }
 
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+template <int NX, bool kBF16Out>
+__device__ __forceinline__ void store_row(const float (&v)[NX], const float* __restrict__ Cin,
+                                          void* __restrict__ Dout, int M, int N, int64_t n) {
+  if (n >= N) return;
+#pragma unroll
+  for (int mm = 0; mm < NX; ++mm) {
+    if (mm < M) {
+      float o = v[mm];
+      if (Cin != nullptr) o += __ldg(Cin + static_cast<int64_t>(mm) * N + n);
+      if (kBF16Out)
+        static_cast<__nv_bfloat16*>(Dout)[static_cast<int64_t>(mm) * N + n] = __float2bfloat16_rn(o);
+      else
+        static_cast<float*>(Dout)[static_cast<int64_t>(mm) * N + n] = o;
+    }
+  }
+}
+
 template <int NX, int CH, bool kBF16Out>
 __global__ void __launch_bounds__(kDecThreads, 1)
     gemm_mxfp4_decode_kernel(const __grid_constant__ CUtensorMap tmX,
@@ -369,8 +401,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                              float* __restrict__ ws, uint32_t* __restrict__ counters) {
   constexpr int kStages = Cfg<NX, CH>::kStages;
   constexpr int kSfCols = Cfg<NX, CH>::kSfColsPerStage;
-  constexpr int kAccCols = Cfg<NX, CH>::kAccCols;
   constexpr int kSfBase = Cfg<NX, CH>::kSfBase;
+  constexpr int kTmemCols = Cfg<NX, CH>::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
   Smem<NX, CH>& sm = *reinterpret_cast<Smem<NX, CH>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -385,7 +417,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&sm.full[s]), 1);
+      mbar_init(smem_u32(&sm.full[s]), 1 + 4);   // producer + four scale writers
       mbar_init(smem_u32(&sm.empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -410,6 +442,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const uint32_t tmem = sm.tmem_base;
 
   if (warp == kProducerWarp) {
+    // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t keep = l2_policy_evict_last();    // activations: re-read by every CTA
       const uint64_t stream = l2_policy_evict_first(); // weights: read exactly once
@@ -424,10 +457,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         const int64_t tile = u / KS;
         const int c0 = static_cast<int>(u % KS) * CH;    // first 128-byte chunk
-        const int ka0 = 2 * c0;
-        const int na = min(2 * CH, KA - ka0);
         const uint32_t fb = smem_u32(&sm.full[s]);
-        mbar_arrive_expect_tx(fb, CH * (128 + NX) * kRowBytes + 2 * na * kSfAtom);
+        mbar_arrive_expect_tx(fb, CH * (128 + NX) * kRowBytes);
         if (CH == 1) {
           tma_load_2d_hint(smem_u32(sm.w[s]), &tmW, fb, c0 * kRowBytes, static_cast<int32_t>(tile * 128), stream);
           tma_load_2d_hint(smem_u32(sm.x[s]), &tmX, fb, c0 * kRowBytes, 0, keep);
@@ -435,13 +466,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           tma_load_3d_hint(smem_u32(sm.w[s]), &tmW, fb, 0, static_cast<int32_t>(tile * 128), c0, stream);
           tma_load_3d_hint(smem_u32(sm.x[s]), &tmX, fb, 0, 0, c0, keep);
         }
-        bulk_load(smem_u32(sm.sfw[s]), sfW + (tile * KA + ka0) * kSfAtom, na * kSfAtom, fb);
-        bulk_load(smem_u32(sm.sfx[s]), sfX + static_cast<int64_t>(ka0) * kSfAtom, na * kSfAtom, fb);
       }
       drain_fills(sm.full, kStages, it);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
+    // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
       uint32_t it = 0, seg = 0;
       for (int64_t u = u0; u < u1; ++u, ++it) {
@@ -452,9 +482,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const bool last = (u == u1 - 1) || ks == KS - 1;
         const uint32_t buf = seg & 1u;
         if (sm.abort_flag) break;
-        // completion k of tempty[buf] = the k-th time the epilogue handed the
-        // (zeroed) buffer back; completion 0 is the initial zeroing
-        if (first && !mbar_wait(smem_u32(&sm.tempty[buf]), (seg >> 1) & 1u)) {
+        // use n = seg / 2 of this buffer waits for the epilogue's n-th hand-
+        // back (the first use of each buffer passes at once)
+        if (first && !mbar_wait(smem_u32(&sm.tempty[buf]), ((seg >> 1) & 1u) ^ 1u)) {
           raise_abort(&sm.abort_flag);
           break;
         }
@@ -464,27 +494,38 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         tc_fence_after();
         const int c0 = ks * CH;
-        const int ka0 = 2 * c0;
-        const int na = min(2 * CH, KA - ka0);
         const uint32_t sfc = tmem + kSfBase + s * kSfCols;
-        const uint32_t d = tmem + buf * kAccCols;
-        for (int a = 0; a < na; ++a) {
-          tc_cp_32x128b_warpx4(sfc + 16 * (a >> 1) + 4 * (a & 1),
-                               sdesc_sf_32x16(smem_u32(sm.sfw[s] + a * kSfAtom)));
-          tc_cp_32x128b_warpx4(sfc + 16 * (a >> 1) + 8 + 4 * (a & 1),
-                               sdesc_sf_32x16(smem_u32(sm.sfx[s] + a * kSfAtom)));
-        }
-        const int nch = min(CH, KC - c0);
-        for (int j = 0; j < nch; ++j) {
-          const uint64_t wd = sdesc_kmajor_sw128(smem_u32(sm.w[s] + j * kSlab));
-          const uint64_t xd = sdesc_kmajor_sw128(smem_u32(sm.x[s] + j * NX * kRowBytes));
-          const int rem = kbytes - (c0 + j) * kRowBytes;
-          const int nk = min(4, (rem + 31) / 32);
-          const uint32_t sfj = sfc + 16 * j;
-          for (int kk = 0; kk < nk; ++kk) {
-            const uint32_t id = idesc_mxf4(128, NX, (kk & 1) * 2, (kk & 1) * 2);
-            mma_mxf4(d + (kk % kAcc) * NX, wd + 2 * kk, xd + 2 * kk, id, sfj + 4 * (kk >> 1),
-                     sfj + 8 + 4 * (kk >> 1), 1u);
+        const uint32_t d = tmem + buf * NX;
+        // the first MMA of a segment overwrites the accumulator
+        const uint32_t acc0 = first ? 0u : 1u;
+        if ((c0 + CH) * kRowBytes <= kbytes) {
+          // whole stage: fully unrolled so the MMAs issue back to back
+          // (descriptor start addresses advance in 16-byte units)
+          const uint64_t w0 = sdesc_kmajor_sw128(smem_u32(sm.w[s]));
+          const uint64_t x0 = sdesc_kmajor_sw128(smem_u32(sm.x[s]));
+#pragma unroll
+          for (int j = 0; j < CH; ++j) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              mma_mxf4(d, w0 + (j * kSlab) / 16 + 2 * kk, x0 + (j * NX * kRowBytes) / 16 + 2 * kk,
+                       idesc_mxf4(128, NX, (kk & 1) * 2, (kk & 1) * 2),
+                       sfc + 16 * j + 4 * (kk >> 1), sfc + 16 * j + 8 + 4 * (kk >> 1),
+                       (j == 0 && kk == 0) ? acc0 : 1u);
+            }
+          }
+        } else {
+          const int nch = min(CH, KC - c0);
+          for (int j = 0; j < nch; ++j) {
+            const uint64_t wd = sdesc_kmajor_sw128(smem_u32(sm.w[s] + j * kSlab));
+            const uint64_t xd = sdesc_kmajor_sw128(smem_u32(sm.x[s] + j * NX * kRowBytes));
+            const int rem = kbytes - (c0 + j) * kRowBytes;
+            const int nk = min(4, (rem + 31) / 32);
+            const uint32_t sfj = sfc + 16 * j;
+            for (int kk = 0; kk < nk; ++kk) {
+              const uint32_t id = idesc_mxf4(128, NX, (kk & 1) * 2, (kk & 1) * 2);
+              mma_mxf4(d, wd + 2 * kk, xd + 2 * kk, id, sfj + 4 * (kk >> 1), sfj + 8 + 4 * (kk >> 1),
+                       (j == 0 && kk == 0) ? acc0 : 1u);
+            }
           }
         }
         tc_commit(smem_u32(&sm.empty[s]));
@@ -497,24 +538,55 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       if (!mbar_wait(smem_u32(&sm.final_bar), 0)) raise_abort(&sm.abort_flag);
     }
     __syncwarp();
+  } else if (warp >= kSfWarp0) {
+    // ----------------------------------------------------- scale writers
+    // Each warp stores the stage's scale atoms into its own quarter of the
+    // tensor-memory lanes with tcgen05.st: lane l of every quarter holds
+    // bytes [16 l, 16 l + 16) of an atom in four consecutive columns, the
+    // image a 32x128b.warpx4 copy would make.  Keeping these stores off the
+    // tensor pipe lets the MMAs issue back to back.  A stage's columns are
+    // rewritten only after its previous MMAs completed (empty barrier).
+    const uint32_t lane_base = tmem + ((static_cast<uint32_t>(warp & 3) * 32u) << 16);
+    uint32_t it = 0;
+    for (int64_t u = u0; u < u1; ++u, ++it) {
+      const int s = static_cast<int>(it % kStages);
+      const uint32_t ph = (it / kStages) & 1u;
+      if (sm.abort_flag) break;
+      if (!mbar_wait(smem_u32(&sm.empty[s]), ph ^ 1u)) {
+        raise_abort(&sm.abort_flag);
+        break;
+      }
+      tc_fence_after();
+      const int64_t tile = u / KS;
+      const int ka0 = 2 * static_cast<int>(u % KS) * CH;
+      const int na = min(2 * CH, KA - ka0);
+      const uint4* gw = reinterpret_cast<const uint4*>(sfW + (tile * KA + ka0) * kSfAtom) + lane;
+      const uint4* gx = reinterpret_cast<const uint4*>(sfX + static_cast<int64_t>(ka0) * kSfAtom) + lane;
+      uint4 vw[2 * CH], vx[2 * CH];
+#pragma unroll
+      for (int a = 0; a < 2 * CH; ++a) {
+        if (a < na) {
+          vw[a] = __ldg(gw + a * (kSfAtom / 16));
+          vx[a] = __ldg(gx + a * (kSfAtom / 16));
+        }
+      }
+      const uint32_t sfc = lane_base + kSfBase + s * kSfCols;
+#pragma unroll
+      for (int a = 0; a < 2 * CH; ++a) {
+        if (a < na) {
+          tmem_st_4(sfc + 16 * (a >> 1) + 4 * (a & 1), vw[a]);
+          tmem_st_4(sfc + 16 * (a >> 1) + 8 + 4 * (a & 1), vx[a]);
+        }
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.full[s]));
+    }
   } else {
     // ---------------------------------------------------------- epilogue
     const int row = warp * 32 + lane;               // weight row within the tile
     const uint32_t lane_taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    {
-      // zero both accumulator buffers and hand them to the MMA thread
-      uint32_t z[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) z[j] = 0u;
-      for (int c = 0; c < 2 * kAccCols; c += 16) tmem_st_16(lane_taddr + c, z);
-      tc_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&sm.tempty[0]));
-        mbar_arrive(smem_u32(&sm.tempty[1]));
-      }
-    }
     uint32_t seg = 0;
     int64_t u = u0;
     while (u < u1) {
@@ -522,61 +594,91 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const int64_t seg_end = min(u1, (tile + 1) * KS);
       const bool whole = (u == tile * KS) && (seg_end == (tile + 1) * KS);
       const uint32_t buf = seg & 1u;
+      const int64_t n = tile * 128 + row;
+      // Split tile: this CTA holds segment sidx of nseg.  If the other
+      // segments are already published (their counter increments are
+      // visible), this CTA finishes the tile straight from its registers
+      // and skips publishing its own partial.  Otherwise it publishes, and
+      // the last contributor adds the partials.  Either way the partials are
+      // added in segment order, so the result does not depend on timing.
+      int64_t nseg = 1, sidx = 0;
+      int nsuf = 0;
+      bool fast = false;
+      float pre[NX], suf[2][NX];
+      if (!whole) {
+        const int64_t first_owner = owner(tile * KS, U, G);
+        nseg = owner((tile + 1) * KS - 1, U, G) - first_owner + 1;
+        sidx = static_cast<int64_t>(blockIdx.x) - first_owner;
+        nsuf = static_cast<int>(nseg - 1 - sidx);
+        if (nsuf <= 2) {
+          if (threadIdx.x == 0)
+            sm.fast_flag = (ld_acquire_u32(counters + tile) + 1u == static_cast<uint32_t>(nseg)) ? 1u : 0u;
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          fast = sm.fast_flag != 0u;
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (fast) {
+            const float* base = ws + tile * smax * NX * 128 + row;
+#pragma unroll
+            for (int mm = 0; mm < NX; ++mm) pre[mm] = 0.0f;
+            for (int64_t sg = 0; sg < sidx; ++sg) {
+#pragma unroll
+              for (int mm = 0; mm < NX; ++mm) pre[mm] += __ldcg(base + (sg * NX + mm) * 128);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              if (i < nsuf) {
+#pragma unroll
+                for (int mm = 0; mm < NX; ++mm) suf[i][mm] = __ldcg(base + ((sidx + 1 + i) * NX + mm) * 128);
+              }
+            }
+          }
+        }
+      }
       if (sm.abort_flag || !mbar_wait(smem_u32(&sm.tfull[buf]), (seg >> 1) & 1u)) {
         if (!sm.abort_flag) raise_abort(&sm.abort_flag);
         break;
       }
       tc_fence_after();
       float acc[NX];
-      {
-        const uint32_t taddr = lane_taddr + buf * kAccCols;
-        uint32_t z[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) z[j] = 0u;
+      for (int c = 0; c < NX / 16; ++c) {
+        uint32_t r[16];
+        tmem_ld_16(lane_taddr + buf * NX + c * 16, r);
+        tc_wait_ld_16(r);
 #pragma unroll
-        for (int c = 0; c < NX / 16; ++c) {
-#pragma unroll
-          for (int a = 0; a < kAcc; ++a) {
-            uint32_t r[16];
-            tmem_ld_16(taddr + a * NX + c * 16, r);
-            tc_wait_ld_16(r);
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              acc[c * 16 + j] = (a == 0 ? 0.0f : acc[c * 16 + j]) + __uint_as_float(r[j]);
-            tmem_st_16(taddr + a * NX + c * 16, z);    // zero for the next segment
-          }
-        }
-        tc_wait_st();
+        for (int j = 0; j < 16; ++j) acc[c * 16 + j] = __uint_as_float(r[j]);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.tempty[buf]));
-      const int64_t n = tile * 128 + row;
       if (whole) {
-        if (n < N) {
+        store_row<NX, kBF16Out>(acc, Cin, Dout, M, N, n);
+      } else if (fast) {
+        float tot[NX];
 #pragma unroll
-          for (int mm = 0; mm < NX; ++mm) {
-            if (mm < M) {
-              float v = acc[mm];
-              if (Cin != nullptr) v += __ldg(Cin + static_cast<int64_t>(mm) * N + n);
-              if (kBF16Out)
-                static_cast<__nv_bfloat16*>(Dout)[static_cast<int64_t>(mm) * N + n] = __float2bfloat16_rn(v);
-              else
-                static_cast<float*>(Dout)[static_cast<int64_t>(mm) * N + n] = v;
-            }
-          }
+        for (int mm = 0; mm < NX; ++mm) {
+          tot[mm] = pre[mm] + acc[mm];
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            if (i < nsuf) tot[mm] += suf[i][mm];
         }
+        store_row<NX, kBF16Out>(tot, Cin, Dout, M, N, n);
+        // leave the workspace zero-filled for the next call
+        float* base = ws + tile * smax * NX * 128 + row;
+        for (int64_t sg = 0; sg < nseg; ++sg) {
+          if (sg == sidx) continue;
+#pragma unroll
+          for (int mm = 0; mm < NX; ++mm) base[(sg * NX + mm) * 128] = 0.0f;
+        }
+        if (threadIdx.x == 0) atomicExch(counters + tile, 0u);
       } else {
-        const int64_t first_owner = owner(tile * KS, U, G);
-        const int64_t nseg = owner((tile + 1) * KS - 1, U, G) - first_owner + 1;
-        const int64_t sidx = static_cast<int64_t>(blockIdx.x) - first_owner;
         float* part = ws + (tile * smax + sidx) * NX * 128;
 #pragma unroll
         for (int mm = 0; mm < NX; ++mm) part[mm * 128 + row] = acc[mm];
         __threadfence();
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (threadIdx.x == 0) {
-          const uint32_t prev = atomicAdd(&counters[tile], 1u);
+          const uint32_t prev = atomicAdd(counters + tile, 1u);
           sm.last_flag = (prev + 1 == static_cast<uint32_t>(nseg)) ? 1u : 0u;
           // a counter past its segment count means the workspace was not zero
           if (prev + 1 > static_cast<uint32_t>(nseg)) atomicOr(&g_mxfp4_error, kErrWorkspace);
@@ -584,8 +686,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (sm.last_flag) {
           __threadfence();
-          // Sum the segments in order (deterministic), then zero every slot
-          // of this row so the workspace is left zero-filled for any shape.
+          // Sum the segments in order, then zero every slot of this row so
+          // the workspace is left zero-filled for any shape.
           float* base = ws + tile * smax * NX * 128 + row;
           float tot[NX];
 #pragma unroll
@@ -598,20 +700,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
               *slot = 0.0f;
             }
           }
-          if (n < N) {
-#pragma unroll
-            for (int mm = 0; mm < NX; ++mm) {
-              if (mm < M) {
-                float v = tot[mm];
-                if (Cin != nullptr) v += __ldg(Cin + static_cast<int64_t>(mm) * N + n);
-                if (kBF16Out)
-                  static_cast<__nv_bfloat16*>(Dout)[static_cast<int64_t>(mm) * N + n] = __float2bfloat16_rn(v);
-                else
-                  static_cast<float*>(Dout)[static_cast<int64_t>(mm) * N + n] = v;
-              }
-            }
-          }
-          if (threadIdx.x == 0) atomicExch(&counters[tile], 0u);
+          store_row<NX, kBF16Out>(tot, Cin, Dout, M, N, n);
+          if (threadIdx.x == 0) atomicExch(counters + tile, 0u);
         }
       }
       u = seg_end;
@@ -669,10 +759,9 @@ cudaError_t launch_gemm_mxfp4(const Mxfp4GemmArgs& a, int num_sms, cudaStream_t 
 }
 
 size_t gemm_mxfp4_decode_workspace(int M, int N, int K, int num_sms) {
-  const decode::Plan p = decode::make_plan(N, K, num_sms);
+  const decode::Plan p = decode::make_plan(M, N, K, num_sms);
   if (p.smax <= 1) return 0;
-  const int nx = M <= 16 ? 16 : 32;
-  const size_t floats = static_cast<size_t>(p.tiles * p.smax * nx * 128);
+  const size_t floats = static_cast<size_t>(p.tiles * p.smax * p.nx * 128);
   return floats * sizeof(float) + static_cast<size_t>(p.tiles) * sizeof(uint32_t);
 }
 
@@ -702,22 +791,23 @@ cudaError_t launch_decode_variant(const Mxfp4GemmArgs& a, const decode::Plan& p,
 
 cudaError_t launch_gemm_mxfp4_decode(const Mxfp4GemmArgs& a, int num_sms, cudaStream_t s) {
   using namespace decode;
-  const Plan p = make_plan(a.N, a.K, num_sms);
-  const int nx = a.M <= 16 ? 16 : 32;
+  const Plan p = make_plan(a.M, a.N, a.K, num_sms);
   float* ws = static_cast<float*>(a.workspace);
   uint32_t* counters =
-      ws == nullptr ? nullptr : reinterpret_cast<uint32_t*>(ws + p.tiles * p.smax * nx * 128);
-  const int key = (nx == 16 ? 0 : 4) | (p.ch == 1 ? 0 : 2) | (a.out_bf16 ? 1 : 0);
-  switch (key) {
-    case 0: return launch_decode_variant<16, 1, false>(a, p, ws, counters, s);
-    case 1: return launch_decode_variant<16, 1, true>(a, p, ws, counters, s);
-    case 2: return launch_decode_variant<16, kChunksWide, false>(a, p, ws, counters, s);
-    case 3: return launch_decode_variant<16, kChunksWide, true>(a, p, ws, counters, s);
-    case 4: return launch_decode_variant<32, 1, false>(a, p, ws, counters, s);
-    case 5: return launch_decode_variant<32, 1, true>(a, p, ws, counters, s);
-    case 6: return launch_decode_variant<32, kChunksWide, false>(a, p, ws, counters, s);
-    default: return launch_decode_variant<32, kChunksWide, true>(a, p, ws, counters, s);
+      ws == nullptr ? nullptr : reinterpret_cast<uint32_t*>(ws + p.tiles * p.smax * p.nx * 128);
+  const bool bf = a.out_bf16;
+  if (p.nx == 16) {
+    if (p.ch == 1)
+      return bf ? launch_decode_variant<16, 1, true>(a, p, ws, counters, s)
+                : launch_decode_variant<16, 1, false>(a, p, ws, counters, s);
+    return bf ? launch_decode_variant<16, 4, true>(a, p, ws, counters, s)
+              : launch_decode_variant<16, 4, false>(a, p, ws, counters, s);
   }
+  if (p.ch == 1)
+    return bf ? launch_decode_variant<32, 1, true>(a, p, ws, counters, s)
+              : launch_decode_variant<32, 1, false>(a, p, ws, counters, s);
+  return bf ? launch_decode_variant<32, 2, true>(a, p, ws, counters, s)
+            : launch_decode_variant<32, 2, false>(a, p, ws, counters, s);
 }
 
 }  // namespace bsg

@@ -52,7 +52,7 @@ def test_mxfp4_bf16_with_addend():
 
 
 @pytest.mark.parametrize("M", [1, 7, 16, 17, 32])
-@pytest.mark.parametrize("N,K", [(1000, 1024), (4096, 8192), (384, 96)])
+@pytest.mark.parametrize("N,K", [(1000, 1024), (4096, 8192), (384, 96), (2048, 2304), (1536, 768)])
 def test_decode_path(M, N, K):
     A, B = synth.make("decode", m=M, n=N, k=K)
     report(f"decode M={M} N={N} K={K}", *_run(A, B, "bf16", a_bf16=True))
@@ -64,3 +64,30 @@ def test_decode_with_addend_fp32_twice():
     C = synth.addend("decode", 16, 2048)
     report("decode + C (1)", *_run(A, B, "f32", C=C, a_bf16=True))
     report("decode + C (2)", *_run(A, B, "f32", C=C, a_bf16=True))
+
+
+@pytest.mark.parametrize("M", [1, 16, 32])
+def test_decode_full_size_sampled_columns(M):
+    # The decode benchmark shape (N=28672, K=8192), launched exactly as the
+    # benchmark launches it; the oracle checks a sample of output columns
+    # (weight rows) that covers tile edges and split-K segment boundaries.
+    import torch
+    import fp4_gemm_gb300 as bsg
+    dev = device()
+    N, K = 28672, 8192
+    A, B = synth.make("decode", m=M, n=N, k=K)
+    A = synth.bf16_bits_to_f32(synth.to_bf16_bits(A))
+    pa, fa = bsg.bsg_quantize_mxfp4(to_dev(A, dev).to(torch.bfloat16), "tcgen05")
+    pb, fb = bsg.bsg_quantize_mxfp4(to_dev(B, dev), "tcgen05")
+    D = bsg.bsg_gemm(pa, "e2m1", fa, "mx", pb, "e2m1", fb, "mx", out="bf16")
+    assert bsg.bsg_device_error() == 0
+    rng = np.random.default_rng(7)
+    cols = np.unique(np.concatenate([np.arange(0, 4), np.arange(124, 132), np.arange(N - 4, N),
+                                     np.arange(128, N, 128 * 37), rng.integers(0, N, 256)]))
+    opa, ofa = oq.quantize_mxfp4(A)
+    opb, ofb = oq.quantize_mxfp4(B[cols])
+    assert np.array_equal(pa.cpu().numpy(), opa)
+    assert np.array_equal(pb.cpu().numpy()[cols], opb)
+    Dref, bnd = og.gemm_mxfp4(opa, ofa, opb, ofb)
+    Dg = D.float().cpu().numpy()[:, cols]
+    report(f"decode full size M={M} ({cols.size} columns)", *og.within_tolerance(Dg, Dref, bnd, bf16=True))
