@@ -16,11 +16,15 @@ Workloads (synthetic, seeded; see synth/):
   fp8_256, mxfp4_1024   the small parity configurations (latency-bound).
 
 One JSON line is printed by rank 0.  Timing: W warm-up steps, then K steps.
-The step (quantise + GEMM) is captured once as a CUDA graph; each timed step
-is one replay bracketed by CUDA events on the launching stream, with an L2
-flush before it, outside the events (a 256 MB write, then a 256 MB read so
-no dirty lines are left to evict inside the timed step).  The GEMM alone is
-captured and timed the same way for K more replays (roofline).  `e2e` repeats the step through the same API
+For the three full-size workloads every input and output exists in several
+copies (together more than twice the 129 MB L2) and consecutive steps use
+consecutive copies, so no step finds its data in L2; the K steps run back to
+back as replays of a CUDA graph of one step per copy, and one pair of CUDA
+events on the launching stream brackets all of them.  The small parity
+configurations fit in L2 many times over, so each of their steps is one graph
+replay bracketed by events with an L2 flush before it (a 256 MB write, then a
+256 MB read), outside the events.  The GEMM alone is timed the same way for K
+more steps (roofline).  `e2e` repeats the step through the same API
 with the activations copied from pinned host memory and the output copied back
 inside the timed region.  `cpu_baseline` times the CPU oracle on a bounded
 sample of the same workload.  Under torchrun every rank runs an independent
@@ -49,6 +53,7 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # nominal dense ratios to BF16 (2.25 PF): FP8 4.5 PF, FP4 13.5 PF
 RATIO = {"fp8": 2.0, "fp4": 6.0}
 L2_FLUSH_BYTES = 256 << 20
+L2_BYTES = 129 << 20
 
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -130,39 +135,51 @@ class Workload:
             self.A_host_t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
         else:
             self.A_host_t = torch.from_numpy(A).pin_memory()
-        self.A = self.A_host_t.to(dev)
+        A0 = self.A_host_t.to(dev)
         Bt = torch.from_numpy(B).to(dev)
         # weights are quantised once, outside the step (static parameters)
         if self.fp4:
-            self.qb, self.sb = bsg.bsg_quantize_mxfp4(Bt, "tcgen05")
+            qb, sb = bsg.bsg_quantize_mxfp4(Bt, "tcgen05")
         else:
-            self.qb, self.sb = bsg.bsg_quantize_fp8(Bt, self.fb, self.gb)
+            qb, sb = bsg.bsg_quantize_fp8(Bt, self.fb, self.gb)
         del Bt
-        # step buffers (allocated once)
-        if self.fp4:
-            self.qa, self.sa = bsg.bsg_quantize_mxfp4(self.A, "tcgen05")
-        else:
-            self.qa, self.sa = bsg.bsg_quantize_fp8(self.A, self.fa, self.ga)
-        self.D = torch.empty((M, N), dtype=torch.bfloat16 if self.out == "bf16" else torch.float32,
-                             device=dev)
+        # Timed steps cycle over `sets` copies of every input and output, so
+        # no step finds its data in L2 (the copies together exceed twice the
+        # 129 MB L2); tiny workloads use one set and an explicit L2 flush.
+        touched = self.step_bytes()
+        self.rotating = touched >= (8 << 20)
+        self.nsets = max(2, -(-2 * L2_BYTES // int(touched)) + 1) if self.rotating else 1
+        self.sets = []
+        for r in range(self.nsets):
+            st = {"A": A0 if r == 0 else A0.clone(),
+                  "qb": qb if r == 0 else qb.clone(), "sb": sb if r == 0 else sb.clone()}
+            if self.fp4:
+                st["qa"], st["sa"] = bsg.bsg_quantize_mxfp4(st["A"], "tcgen05")
+            else:
+                st["qa"], st["sa"] = bsg.bsg_quantize_fp8(st["A"], self.fa, self.ga)
+            st["D"] = torch.empty((M, N), dtype=torch.bfloat16 if self.out == "bf16" else torch.float32,
+                                  device=dev)
+            self.sets.append(st)
+        self.A, self.D = self.sets[0]["A"], self.sets[0]["D"]
         self.D_host = torch.empty_like(self.D, device="cpu").pin_memory()
         self.ws = bsg.workspace_for(M, N, K, self.fa, self.fb, dev)
         torch.cuda.synchronize()
 
-    def quantize(self):
-        b = self.bsg
+    def quantize(self, r=0):
+        b, st = self.bsg, self.sets[r]
         if self.fp4:
-            b.bsg_quantize_mxfp4(self.A, "tcgen05", q=self.qa, sf=self.sa)
+            b.bsg_quantize_mxfp4(st["A"], "tcgen05", q=st["qa"], sf=st["sa"])
         else:
-            b.bsg_quantize_fp8(self.A, self.fa, self.ga, q=self.qa, scales=self.sa)
+            b.bsg_quantize_fp8(st["A"], self.fa, self.ga, q=st["qa"], scales=st["sa"])
 
-    def gemm(self):
-        self.bsg.bsg_gemm(self.qa, self.fa, self.sa, self.ga, self.qb, self.fb, self.sb, self.gb,
-                          out=self.out, D=self.D, workspace=self.ws, K=self.K)
+    def gemm(self, r=0):
+        st = self.sets[r]
+        self.bsg.bsg_gemm(st["qa"], self.fa, st["sa"], self.ga, st["qb"], self.fb, st["sb"], self.gb,
+                          out=self.out, D=st["D"], workspace=self.ws, K=self.K)
 
-    def step(self):
-        self.quantize()
-        self.gemm()
+    def step(self, r=0):
+        self.quantize(r)
+        self.gemm(r)
 
     launches_per_step = 2
 
@@ -378,61 +395,95 @@ def main():
         torch.cuda.current_stream().wait_stream(side)
         return g
 
-    g_step = capture(w.step)
-    g_gemm = capture(w.gemm)
+    K = args.steps
+    R = w.nsets
+    if w.rotating:
+        # one graph runs R consecutive steps, each on its own input set
+        g_step = capture(lambda: [w.step(r) for r in range(R)])
+        g_gemm = capture(lambda: [w.gemm(r) for r in range(R)])
+        reps = -(-K // R)
+    else:
+        g_step = capture(w.step)
+        g_gemm = capture(w.gemm)
+        reps = K
+    K = reps * R if w.rotating else K
     for _ in range(2):
         g_step.replay()
         g_gemm.replay()
     torch.cuda.synchronize()
 
-    K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     clocks = Clocks(local)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
     t_wall0 = time.perf_counter()
-    for i in range(K):
-        flush_l2(i)                                 # outside the events
-        ev[i][0].record(stream)
-        g_step.replay()
-        ev[i][1].record(stream)
-    for i in range(K):
-        flush_l2(i)
-        ev[i][2].record(stream)
-        g_gemm.replay()
-        ev[i][3].record(stream)
-    torch.cuda.synchronize()
+    if w.rotating:
+        # back-to-back replays; the whole timed region is one event pair
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev[0].record(stream)
+        for _ in range(reps):
+            g_step.replay()
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        ev[2].record(stream)
+        for _ in range(reps):
+            g_gemm.replay()
+        ev[3].record(stream)
+        torch.cuda.synchronize()
+        step_total = ev[0].elapsed_time(ev[1])
+        gemm_total = ev[2].elapsed_time(ev[3])
+        step_ms_mean = step_total / K
+        gemm_ms_mean = gemm_total / K
+        gemm_ms_min = gemm_ms_mean
+    else:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+        for i in range(K):
+            flush_l2(i)                                 # outside the events
+            ev[i][0].record(stream)
+            g_step.replay()
+            ev[i][1].record(stream)
+        for i in range(K):
+            flush_l2(i)
+            ev[i][2].record(stream)
+            g_gemm.replay()
+            ev[i][3].record(stream)
+        torch.cuda.synchronize()
+        step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+        gemm_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
+        step_ms_mean = statistics.mean(step_ms)
+        gemm_ms_mean = statistics.mean(gemm_ms)
+        gemm_ms_min = min(gemm_ms)
     wall = time.perf_counter() - t_wall0
     clk = clocks.stop()
     if bsg.bsg_device_error() != 0:
         raise RuntimeError("device error during the timed steps")
-    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    gemm_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
-    quant_ms = [max(a - b, 0.0) for a, b in zip(step_ms, gemm_ms)]
-    ms = statistics.mean(step_ms)
+    ms = step_ms_mean
     if dist is not None:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
 
-    # end to end through the API with host buffers
+    # end to end through the API with host buffers (rotating over the same
+    # input sets as the device-timed steps)
     e2e = None
     if not args.no_e2e:
         h2d = w.A_host_t.numel() * w.A_host_t.element_size()
         d2h = w.D.numel() * w.D.element_size()
-        for _ in range(2):
-            w.A.copy_(w.A_host_t, non_blocking=True)
-            w.step()
-            w.D_host.copy_(w.D, non_blocking=True)
+
+        def e2e_step(i):
+            st = w.sets[i % R]
+            st["A"].copy_(w.A_host_t, non_blocking=True)
+            w.step(i % R)
+            w.D_host.copy_(st["D"], non_blocking=True)
+
+        for i in range(2 * R):
+            e2e_step(i)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(K):
-            w.A.copy_(w.A_host_t, non_blocking=True)
-            w.step()
-            w.D_host.copy_(w.D, non_blocking=True)
+        for i in range(K):
+            e2e_step(i)
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1) / K
@@ -445,7 +496,7 @@ def main():
                "ms_per_step": e_ms}
 
     pk, pk_kind = peaks()
-    g_s = statistics.mean(gemm_ms) / 1e3
+    g_s = gemm_ms_mean / 1e3
     if w.name == "decode":
         achieved = w.gemm_bytes() / g_s / 1e9
         peak = pk["hbm_gbs"]
@@ -472,14 +523,18 @@ def main():
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
                    "a": f"{w.fa}/{w.ga}", "b": f"{w.fb}/{w.gb}", "out": w.out,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "flushed before every timed step (256 MB write, then a 256 MB read)",
-                   "timing": "CUDA events around a CUDA-graph replay of each step"},
-        "quantize_ms": statistics.mean(quant_ms), "gemm_ms": statistics.mean(gemm_ms),
-        "gemm_ms_min": min(gemm_ms),
+                   "l2": (f"inputs rotate over {R} copies ({R} x {w.step_bytes() / 1e6:.0f} MB > L2): "
+                          "no step finds its data in L2" if w.rotating else
+                          "flushed before every timed step (256 MB write, then a 256 MB read)"),
+                   "timing": ("one CUDA-event pair around K back-to-back steps (CUDA graphs of "
+                              f"{R} steps replayed)" if w.rotating else
+                              "CUDA events around a CUDA-graph replay of each step")},
+        "quantize_ms": max(step_ms_mean - gemm_ms_mean, 0.0), "gemm_ms": gemm_ms_mean,
+        "gemm_ms_min": gemm_ms_min,
         "wall_s": wall,
         "roofline": roof,
         "clocks": clk,
-        "gpu_launches": (w.launches_per_step + 1) * K,   # step replays + GEMM-only replays
+        "gpu_launches": (w.launches_per_step + 1) * K,   # K steps + K GEMM-only launches
     }
     if e2e is not None:
         line["e2e"] = e2e

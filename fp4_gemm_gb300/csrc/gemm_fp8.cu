@@ -175,6 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (kPair) cluster_sync();    // barriers and tensor memory of both CTAs are ready
   tc_fence_after();
+  grid_dep_launch();
+  grid_dep_wait();
   const uint32_t tmem = sm.tmem_base;
 
   if (warp == kProducerWarp) {
@@ -458,13 +460,15 @@ cudaError_t launch_variant(const Fp8GemmArgs& a, int num_sms, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = per;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;   // the occupancy query below sees the cluster shape only
   if (kPair) {
     // A pair needs two SMs of one GPC; not every SM may find a partner, so a
     // persistent grid is sized by how many pairs can be resident at once.
@@ -485,6 +489,7 @@ cudaError_t launch_variant(const Fp8GemmArgs& a, int num_sms, cudaStream_t s) {
   // keep the smaller operand resident: sweep it inside groups of the larger
   const bool raster_n = static_cast<int64_t>(a.M) < static_cast<int64_t>(a.N);
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.sA, a.sB, a.C, a.D, a.M, a.N, a.K, idesc,
                             vec_out, raster_n);
 }

@@ -127,6 +127,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  grid_dep_launch();
+  grid_dep_wait();
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
@@ -440,6 +442,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  grid_dep_launch();
+  grid_dep_wait();
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------ TMA producer
@@ -743,19 +747,11 @@ cudaError_t launch_gemm_mxfp4(const Mxfp4GemmArgs& a, int num_sms, cudaStream_t 
   const int grid = tiles < num_sms ? tiles : num_sms;
   const bool vec_out = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) &&
                        (a.out_bf16 ? (a.N % 8 == 0) : (a.N % 4 == 0));
-  cudaError_t e;
-  if (a.out_bf16) {
-    e = set_smem(gemm_mxfp4_kernel<true>, smem);
-    if (e != cudaSuccess) return e;
-    gemm_mxfp4_kernel<true><<<grid, kThreads, smem, s>>>(a.tmA, a.tmB, a.sfA, a.sfB, a.C, a.D,
-                                                         a.M, a.N, a.K, vec_out);
-  } else {
-    e = set_smem(gemm_mxfp4_kernel<false>, smem);
-    if (e != cudaSuccess) return e;
-    gemm_mxfp4_kernel<false><<<grid, kThreads, smem, s>>>(a.tmA, a.tmB, a.sfA, a.sfB, a.C, a.D,
-                                                          a.M, a.N, a.K, vec_out);
-  }
-  return cudaGetLastError();
+  auto kern = a.out_bf16 ? gemm_mxfp4_kernel<true> : gemm_mxfp4_kernel<false>;
+  const cudaError_t e = set_smem(kern, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a.tmA, a.tmB, a.sfA, a.sfB, a.C, a.D,
+                    a.M, a.N, a.K, vec_out);
 }
 
 size_t gemm_mxfp4_decode_workspace(int M, int N, int K, int num_sms) {
@@ -783,9 +779,9 @@ cudaError_t launch_decode_variant(const Mxfp4GemmArgs& a, const decode::Plan& p,
   const size_t smem = sizeof(Smem<NX, CH>) + 1024;
   cudaError_t e = set_smem(gemm_mxfp4_decode_kernel<NX, CH, BF>, smem);
   if (e != cudaSuccess) return e;
-  gemm_mxfp4_decode_kernel<NX, CH, BF><<<static_cast<int>(p.G), kDecThreads, smem, s>>>(
-      tmX, tmW, a.sfA, a.sfB, a.C, a.D, a.M, a.N, a.K, p.KS, p.U, p.smax, ws, counters);
-  return cudaGetLastError();
+  return launch_pdl(gemm_mxfp4_decode_kernel<NX, CH, BF>, dim3(static_cast<unsigned>(p.G)),
+                    dim3(kDecThreads), smem, s, tmX, tmW, a.sfA, a.sfB, a.C, a.D, a.M, a.N, a.K, p.KS,
+                    p.U, p.smax, ws, counters);
 }
 }  // namespace
 

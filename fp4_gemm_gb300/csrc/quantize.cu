@@ -94,6 +94,8 @@ template <bool kBF16>
 __global__ void __launch_bounds__(256) quantize_fp8_tile_kernel(
     const void* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, int fmt, float fmt_max,
     bool vec_in, bool vec_out, uint8_t* __restrict__ q, float* __restrict__ scales) {
+  grid_dep_launch();
+  grid_dep_wait();
   __shared__ float warp_max[8];
   __shared__ float tile_scale;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
@@ -145,6 +147,8 @@ template <bool kBF16>
 __global__ void __launch_bounds__(256) quantize_fp8_row_kernel(
     const void* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, int fmt, float fmt_max,
     bool vec_in, bool vec_out, uint8_t* __restrict__ q, float* __restrict__ scales) {
+  grid_dep_launch();
+  grid_dep_wait();
   constexpr int kItems = 4;
   const int64_t kt = (cols + 127) / 128;
   const int64_t total = rows * kt;
@@ -219,6 +223,8 @@ template <bool kBF16, bool kTC>
 __global__ void __launch_bounds__(256) quantize_mxfp4_kernel(
     const void* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, bool vec_in,
     uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  grid_dep_launch();
+  grid_dep_wait();
   const int64_t kb = cols / 32;
   const int64_t kb_pad = kTC ? ((kb + 3) / 4) * 4 : kb;
   const int64_t chunks = (kb_pad + 7) / 8;
@@ -265,6 +271,8 @@ __global__ void __launch_bounds__(256) quantize_mxfp4_kernel(
 
 __global__ void sf_to_tcgen05_kernel(const uint8_t* __restrict__ sf, int64_t rows, int64_t kb,
                                      int64_t total, uint8_t* __restrict__ out) {
+  grid_dep_launch();
+  grid_dep_wait();
   const int64_t off = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (off >= total) return;
   const int64_t groups = (kb + 3) / 4;
@@ -295,13 +303,9 @@ cudaError_t launch_quantize_fp8_tile(const void* x, bool src_bf16, int64_t rows,
   const bool vec_in = src_bf16 ? (aligned(x, 8) && ld % 4 == 0) : (aligned(x, 16) && ld % 4 == 0);
   const bool vec_out = aligned(q, 4) && cols % 4 == 0;
   dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>((rows + 127) / 128));
-  if (src_bf16)
-    quantize_fp8_tile_kernel<true><<<grid, 256, 0, s>>>(x, rows, cols, ld, fmt, fmt_max, vec_in,
-                                                         vec_out, q, scales);
-  else
-    quantize_fp8_tile_kernel<false><<<grid, 256, 0, s>>>(x, rows, cols, ld, fmt, fmt_max, vec_in,
-                                                          vec_out, q, scales);
-  return cudaGetLastError();
+  auto kern = src_bf16 ? quantize_fp8_tile_kernel<true> : quantize_fp8_tile_kernel<false>;
+  return launch_pdl(kern, grid, dim3(256), 0, s, x, rows, cols, ld, fmt, fmt_max, vec_in, vec_out,
+                    q, scales);
 }
 
 cudaError_t launch_quantize_fp8_row(const void* x, bool src_bf16, int64_t rows, int64_t cols,
@@ -311,13 +315,9 @@ cudaError_t launch_quantize_fp8_row(const void* x, bool src_bf16, int64_t rows, 
   const bool vec_out = aligned(q, 4) && cols % 4 == 0;
   const int64_t items = rows * ((cols + 127) / 128);
   const int64_t blocks = (items + 31) / 32;  // 8 warps x 4 items
-  if (src_bf16)
-    quantize_fp8_row_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        x, rows, cols, ld, fmt, fmt_max, vec_in, vec_out, q, scales);
-  else
-    quantize_fp8_row_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        x, rows, cols, ld, fmt, fmt_max, vec_in, vec_out, q, scales);
-  return cudaGetLastError();
+  auto kern = src_bf16 ? quantize_fp8_row_kernel<true> : quantize_fp8_row_kernel<false>;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, x, rows, cols, ld,
+                    fmt, fmt_max, vec_in, vec_out, q, scales);
 }
 
 cudaError_t launch_quantize_mxfp4(const void* x, bool src_bf16, int64_t rows, int64_t cols,
@@ -329,26 +329,16 @@ cudaError_t launch_quantize_mxfp4(const void* x, bool src_bf16, int64_t rows, in
   const int64_t rows_pad = tc_layout ? ((rows + 127) / 128) * 128 : rows;
   const int64_t warps = rows_pad * ((kb_pad + 7) / 8);
   const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
-  if (src_bf16) {
-    if (tc_layout)
-      quantize_mxfp4_kernel<true, true><<<blocks, 256, 0, s>>>(x, rows, cols, ld, vec_in, q, sf);
-    else
-      quantize_mxfp4_kernel<true, false><<<blocks, 256, 0, s>>>(x, rows, cols, ld, vec_in, q, sf);
-  } else {
-    if (tc_layout)
-      quantize_mxfp4_kernel<false, true><<<blocks, 256, 0, s>>>(x, rows, cols, ld, vec_in, q, sf);
-    else
-      quantize_mxfp4_kernel<false, false><<<blocks, 256, 0, s>>>(x, rows, cols, ld, vec_in, q, sf);
-  }
-  return cudaGetLastError();
+  auto kern = src_bf16 ? (tc_layout ? quantize_mxfp4_kernel<true, true> : quantize_mxfp4_kernel<true, false>)
+                       : (tc_layout ? quantize_mxfp4_kernel<false, true> : quantize_mxfp4_kernel<false, false>);
+  return launch_pdl(kern, dim3(blocks), dim3(256), 0, s, x, rows, cols, ld, vec_in, q, sf);
 }
 
 cudaError_t launch_sf_to_tcgen05(const uint8_t* sf, int64_t rows, int64_t kblocks, uint8_t* out,
                                  cudaStream_t s) {
   const int64_t total = ((rows + 127) / 128) * ((kblocks + 3) / 4) * 512;
-  sf_to_tcgen05_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, s>>>(
-      sf, rows, kblocks, total, out);
-  return cudaGetLastError();
+  return launch_pdl(sf_to_tcgen05_kernel, dim3(static_cast<unsigned>((total + 255) / 256)),
+                    dim3(256), 0, s, sf, rows, kblocks, total, out);
 }
 
 }  // namespace bsg
