@@ -3,8 +3,9 @@
 //
 // FP8 ("FP8 GEMM on CDNA4", sections 3.3 and 4.2): each scale group's largest
 // magnitude comes from a warp-shuffle max reduction; s = max_abs / fmt_max in
-// FP32; every element is divided by s (IEEE division) and converted with the
-// hardware's round-to-nearest-even, saturating cvt.
+// FP32; every element is divided by s (correctly rounded FP32 division, see
+// GroupDiv) and converted with the hardware's round-to-nearest-even,
+// saturating cvt.
 //
 // MXFP4 ("Rubin FP4 GEMM deep dive", section 4.2 steps 1-3): per 32-element
 // block v = max_abs / 6 in FP32; the E8M0 scale is the power of two nearest to
@@ -77,6 +78,33 @@ __device__ __forceinline__ float fp8_scale(float amax, float fmt_max) {
   return s == 0.0f ? 1.0f : s;
 }
 
+// Correctly rounded x / s for a whole group that shares the divisor s.
+//
+// Markstein's division with a fused multiply-add (P. Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): with r = RN(1/s) and a faithful quotient q, the residual
+// x - q s is exact and RN(q + (x - q s) r) = RN(x / s).  One correction step
+// from RN(x r) (within 1.5 ulp) first makes q faithful.  The theorem needs
+// every intermediate normal: for s in [2^-80, 2^80] that holds whenever
+// |x / s| >= 2^-18, and smaller quotients become a signed zero in E4M3 and
+// E5M2 whichever way they round, so only their sign is fixed up.  Groups
+// with s outside that range (or not finite) divide with __fdiv_rn.
+struct GroupDiv {
+  float s, r;
+  bool fast;
+  __device__ __forceinline__ explicit GroupDiv(float s_) : s(s_) {
+    fast = s_ >= 0x1p-80f && s_ <= 0x1p80f;
+    r = __frcp_rn(s_);
+  }
+  __device__ __forceinline__ float operator()(float x) const {
+    if (!fast) return __fdiv_rn(x, s);
+    const float q0 = x * r;
+    const float q1 = fmaf(fmaf(-q0, s, x), r, q0);
+    const float q2 = fmaf(fmaf(-q1, s, x), r, q1);
+    return q2 == 0.0f ? x * 0.0f : q2;
+  }
+};
+
 __device__ __forceinline__ void store_codes4(uint8_t* q, int64_t off, int64_t col, int64_t cols,
                                              bool vec_ok, uint32_t codes) {
   if (vec_ok && col + 3 < cols) {
@@ -129,13 +157,12 @@ __global__ void __launch_bounds__(256) quantize_fp8_tile_kernel(
     scales[static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x] = s;
   }
   __syncthreads();
-  const float s = tile_scale;
+  const GroupDiv div(tile_scale);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int64_t row = r0 + rr + 8 * i;
     if (row < rows && col < cols) {
-      const uint32_t c = cvt4_fp8(fmt, __fdiv_rn(v[i][0], s), __fdiv_rn(v[i][1], s),
-                                  __fdiv_rn(v[i][2], s), __fdiv_rn(v[i][3], s));
+      const uint32_t c = cvt4_fp8(fmt, div(v[i][0]), div(v[i][1]), div(v[i][2]), div(v[i][3]));
       store_codes4(q, row * cols + col, col, cols, vec_out, c);
     }
   }
@@ -178,8 +205,8 @@ __global__ void __launch_bounds__(256) quantize_fp8_row_kernel(
     const int64_t col = t * 128 + 4 * lane;
     if (lane == 0) scales[t * rows + row] = s;
     if (col < cols) {
-      const uint32_t c = cvt4_fp8(fmt, __fdiv_rn(v[i][0], s), __fdiv_rn(v[i][1], s),
-                                  __fdiv_rn(v[i][2], s), __fdiv_rn(v[i][3], s));
+      const GroupDiv div(s);
+      const uint32_t c = cvt4_fp8(fmt, div(v[i][0]), div(v[i][1]), div(v[i][2]), div(v[i][3]));
       store_codes4(q, row * cols + col, col, cols, vec_out, c);
     }
   }

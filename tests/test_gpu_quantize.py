@@ -130,3 +130,56 @@ def test_e8m0_rounding_boundaries():
     q, sf = bsg.bsg_quantize_mxfp4(to_dev(x, dev), "rowmajor")
     assert np.array_equal(sf.cpu().numpy(), osf)
     assert np.array_equal(q.cpu().numpy(), op)
+
+
+def _division_stress(fmt, gran, seed):
+    """Groups whose amax spans the FP32 range, filled with values whose
+    quotient by the group scale lies next to an FP8 rounding midpoint, so a
+    quotient off by one FP32 ulp would change the code."""
+    g = np.random.default_rng(seed)
+    fm = oq.fmt_max_default(fmt)
+    table = np.unique(np.abs(formats.decode_table(fmt)[np.isfinite(formats.decode_table(fmt))]))
+    mids = ((table[:-1] + table[1:]) / 2).astype(np.float32)
+    exps = [-126, -110, -95, -88, -81, -80, -79, -60, -20, -1, 0, 1, 20, 60, 79, 80, 81, 100, 120, 127]
+    amaxes = [np.float32(np.ldexp(1.0 + g.random(), e)) if e < 127 else np.float32(3.0e38) for e in exps]
+    groups = len(amaxes)
+    if gran == "tile":
+        x = np.zeros((128, 128 * groups), np.float32)
+        views = [np.zeros(128 * 128, np.float32) for _ in range(groups)]
+    else:
+        x = np.zeros((groups, 128 * 3), np.float32)
+        views = [x[i, 128 * (i % 3):128 * (i % 3 + 1)] for i in range(groups)]
+    for v, amax in zip(views, amaxes):
+        s = oq.fp8_scale(amax, fm)
+        n = v.size
+        m = mids[g.integers(0, mids.size, n)] * np.where(g.random(n) < 0.5, -1, 1).astype(np.float32)
+        with np.errstate(over="ignore", under="ignore"):
+            vals = (m * s).astype(np.float32)
+            step = g.integers(-2, 3, n)
+            vals = np.where(step > 0, np.nextafter(vals, np.float32(np.inf)), vals)
+            vals = np.where(step < 0, np.nextafter(vals, np.float32(-np.inf)), vals).astype(np.float32)
+        vals = np.clip(vals, -amax, amax)
+        vals[: 4] = [amax, -0.0, 0.0, np.float32(1e-45)]
+        vals[4: 8] = -np.float32(np.ldexp(1.0, -140)), np.float32(np.ldexp(1.0, -126)), -amax, amax / 3
+        v[:] = vals
+    if gran == "tile":
+        for i, v in enumerate(views):
+            x[:, 128 * i:128 * (i + 1)] = v.reshape(128, 128)
+    return x
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("gran", ["tile", "row"])
+def test_fp8_division_next_to_rounding_midpoints(fmt, gran):
+    # Every element is divided by its group's scale in FP32 and then rounded
+    # to FP8; these inputs put the FP32 quotient next to FP8 midpoints over
+    # scales from 2^-126 to 2^127, including signed zeros and subnormals.
+    import fp4_gemm_gb300 as bsg
+    dev = device()
+    x = _division_stress(fmt, gran, 11 if gran == "tile" else 12)
+    q, s = bsg.bsg_quantize_fp8(to_dev(x, dev), fmt, gran)
+    oq_, os_ = oq.quantize_fp8(x, fmt, gran)
+    assert np.array_equal(s.cpu().numpy(), os_)
+    got = q.cpu().numpy()
+    bad = np.argwhere(got != oq_)
+    assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[:3].tolist()}"
