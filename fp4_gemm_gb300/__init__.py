@@ -32,7 +32,7 @@ LAYOUT = {"rowmajor": 0, "tcgen05": 1}
 
 EXPORTS = ("bsg_quantize_fp8", "bsg_quantize_mxfp4", "bsg_gemm", "bsg_gemm_workspace_size",
            "bsg_scale_bytes", "bsg_sf_to_tcgen05", "bsg_status_string", "bsg_device_error",
-           "bsg_num_sms", "bsg_gemm_decode_noalloc")
+           "bsg_num_sms", "bsg_gemm_decode_noalloc", "bsg_mma_peak")
 
 
 class BsgError(RuntimeError):
@@ -75,6 +75,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsg_num_sms.restype = i32
     lib.bsg_gemm_decode_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, vp, i32, vp]
     lib.bsg_gemm_decode_noalloc.restype = i32
+    lib.bsg_mma_peak.argtypes = [i32, i32, i64, c.POINTER(i64), vp]
+    lib.bsg_mma_peak.restype = i32
     _lib = lib
     return lib
 
@@ -110,6 +112,17 @@ def bsg_gemm_workspace_size(M: int, N: int, K: int, fa: str, fb: str) -> int:
 
 def bsg_num_sms() -> int:
     return int(load_library().bsg_num_sms())
+
+
+def bsg_mma_peak(fmt: str = "e4m3", pair: bool = False, iters: int = 1 << 16, stream=None) -> int:
+    """Launch the tensor-core throughput microbenchmark on `stream` (or the
+    current stream) and return the FLOPs the launch performs; the caller
+    times it with CUDA events.  fmt "e4m3" (kind::f8f6f4) or "e2m1"
+    (block-scaled kind::mxf4)."""
+    flops = ctypes.c_int64(0)
+    _check(load_library().bsg_mma_peak(FORMAT[fmt], 1 if pair else 0, int(iters),
+                                       ctypes.byref(flops), _stream(stream)), "bsg_mma_peak")
+    return int(flops.value)
 
 
 def bsg_status_string(status: int) -> str:

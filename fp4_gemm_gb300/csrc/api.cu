@@ -59,6 +59,10 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // decode-shaped path (weights streamed once, swap-AB, split-K).
 constexpr int64_t kDecodeMaxM = 32;
 
+// Longest bsg_mma_peak launch: 2^20 iterations of four MMAs run well under
+// the kernels' 2 s wait limit at any clock above 1 GHz.
+constexpr int64_t kMaxPeakIters = int64_t{1} << 20;
+
 }  // namespace
 
 namespace bsg {
@@ -74,6 +78,21 @@ bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t inner_bytes, u
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_out_map(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols, int elem_bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || (elem_bytes != 2 && elem_bytes != 4)) return false;
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || (cols * elem_bytes) % 16 != 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * static_cast<uint64_t>(elem_bytes)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem_bytes), 128};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  return fn(map, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool make_kmajor_map_chunked(CUtensorMap* map, const void* base, uint64_t inner_bytes,
@@ -228,6 +247,8 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
     a.D = D;
     a.out_bf16 = out == BSG_BF16;
     a.pair = bsg::gemm_fp8_use_pair(a.M, a.N, sms);
+    a.tma_out = bsg::make_out_map(&a.tmD, D, static_cast<uint64_t>(M), static_cast<uint64_t>(N),
+                                  out == BSG_BF16 ? 2 : 4);
     if (!make_kmajor_map(&a.tmA, A, K, M, K, 128) ||
         !make_kmajor_map(&a.tmB, B, K, N, K, static_cast<uint32_t>(bsg::gemm_fp8_b_box_rows(a.pair))))
       return BSG_ERR_CUDA;
@@ -266,15 +287,25 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
 bsg_status bsg_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return BSG_ERR_CUDA;
-  uint32_t w0 = 0, w1 = 0, w2 = 0;
+  uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
   if (bsg::quantize_error_read_and_clear(s, &w0) != cudaSuccess ||
       bsg::gemm_fp8_error_read_and_clear(s, &w1) != cudaSuccess ||
-      bsg::gemm_mxfp4_error_read_and_clear(s, &w2) != cudaSuccess)
+      bsg::gemm_mxfp4_error_read_and_clear(s, &w2) != cudaSuccess ||
+      bsg::mma_peak_error_read_and_clear(s, &w3) != cudaSuccess)
     return BSG_ERR_CUDA;
-  const uint32_t w = w0 | w1 | w2;
+  const uint32_t w = w0 | w1 | w2 | w3;
   if (w & 1u) return BSG_ERR_TIMEOUT;
   if (w & 2u) return BSG_ERR_WORKSPACE;
   return BSG_OK;
+}
+
+bsg_status bsg_mma_peak(bsg_format fmt, int pair, int64_t iters, int64_t* flops, void* stream) {
+  if (flops == nullptr || iters <= 0 || iters > kMaxPeakIters) return BSG_ERR_INVALID_ARG;
+  if (fmt != BSG_E4M3 && fmt != BSG_E2M1) return BSG_ERR_UNSUPPORTED;
+  const int sms = num_sms_current();
+  if (sms <= 0 || (pair && sms < 2)) return BSG_ERR_CUDA;
+  return from_cuda(bsg::launch_mma_peak(fmt == BSG_E2M1, pair != 0, iters, sms,
+                                        static_cast<cudaStream_t>(stream), flops));
 }
 
 }  // extern "C"

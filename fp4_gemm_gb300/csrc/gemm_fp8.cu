@@ -17,24 +17,32 @@
 //
 // Two shapes of the same kernel:
 //   * single CTA: 128 x 256 output tiles; per K tile the SM loads A 16 KB +
-//     B 32 KB into a 4-stage ring;
+//     B 32 KB into a 3-stage ring;
 //   * CTA pair (a cluster of two on neighbouring SMs, tcgen05 cta_group::2):
 //     256 x 256 tiles.  Each CTA loads its 128 rows of A and 128 of the 256
-//     rows of B (32 KB per K tile, 6 stages); one thread of the even CTA
+//     rows of B (32 KB per K tile, 4 stages); one thread of the even CTA
 //     issues M = 256 MMAs that read both CTAs' shared memory and write each
 //     CTA's 128 rows of the partial into its own tensor memory.  Per FLOP an
-//     SM moves two thirds of the single-CTA bytes and keeps more K tiles in
-//     flight.
+//     SM moves two thirds of the single-CTA bytes.
 //
 // Warp roles (384 threads = 3 warpgroups, one CTA per SM, persistent):
-//   warp 0     producer: TMA loads of A and B; cp.async of the K tile's
-//              scales into an 8-slot ring.
+//   warp 0     producer: TMA loads of A and B.
 //   warp 1     tensor-memory allocator; MMA issuer (one lane; in a pair only
-//              the even CTA's).
-//   warps 2-3  idle (they complete warpgroup 0).
+//              the even CTA's).  One tcgen05.commit per K tile arrives on
+//              the stage's `done` barrier: it both frees the shared-memory
+//              stage for the producer and hands the partial to the drain.
+//   warp 2     scale loader: cp.async of each K tile's scales into an 8-slot
+//              ring, as far ahead as the ring allows.
+//   warp 3     output store: writes the staged tile to D (TMA tensor stores,
+//              or a bounds-checked copy when D's pitch does not allow TMA).
 //   warps 4-11 promotion + epilogue: warpgroups 1 and 2.  Warp w reads TMEM
 //              lanes 32*(w%4)..+31 (its rows) and column half (w-4)/4 of the
 //              256-wide tile.
+// The promotion warps hand each finished tile to the store warp through a
+// 64 KB shared-memory staging buffer (128-byte swizzled, the TMA layout) and
+// go straight on to the next tile's drain, so the output stores of all SMs
+// (which finish their tiles at the same moments) overlap the next tile's
+// MMAs instead of stalling them.
 // Registers: the kernel launches at 168 per thread (384 x 168 = 64512);
 // warpgroup 0 gives back down to 56 and the promotion warpgroups take 224
 // each, 128 x 56 + 256 x 224 = 64512, which holds 128 FP32 accumulators plus
@@ -57,6 +65,8 @@ constexpr int kScaleSlots = 8;
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
+constexpr int kScaleWarp = 2;
+constexpr int kStoreWarp = 3;
 constexpr int kFirstPromoWarp = 4;
 constexpr int kRegsSmall = 56;     // warpgroup 0 after setmaxnreg.dec
 constexpr int kRegsLarge = 224;    // promotion warpgroups after setmaxnreg.inc
@@ -64,10 +74,23 @@ static_assert(128 * kRegsSmall + 256 * kRegsLarge <= kThreads * 168,
               "register split exceeds the launch allocation");
 constexpr int kTmemCols = 512;     // two 256-column FP32 partial buffers
 constexpr int kGroup = 8;          // tile raster: groups of 8 tiles
+constexpr int kDrainCols = 32;     // TMEM columns per tcgen05.ld in the drain
+
+template <int W>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[W]) {
+  if constexpr (W == 32) tmem_ld_32(taddr, r); else tmem_ld_16(taddr, r);
+}
+template <int W>
+__device__ __forceinline__ void tmem_wait_cols(uint32_t (&r)[W]) {
+  if constexpr (W == 32) tc_wait_ld_32(r); else tc_wait_ld_16(r);
+}
+
+constexpr uint32_t kOutBytes = 64 * 1024;   // output staging
+constexpr uint32_t kOutBlock = 128 * 128;   // one 128-row x 128-byte swizzled box
 
 template <bool kPair>
 struct Cfg {
-  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kStages = kPair ? 4 : 3;
   static constexpr int kBRows = kPair ? BN / 2 : BN;        // B rows this CTA loads
   static constexpr int kTileM = kPair ? 2 * BM : BM;        // rows of a tile
   static constexpr int kPromoArrivals = kPair ? 16 : 8;     // drains per TMEM buffer
@@ -79,15 +102,18 @@ template <bool kPair>
 struct __align__(1024) Smem {
   uint8_t a[Cfg<kPair>::kStages][BM * BK];
   uint8_t b[Cfg<kPair>::kStages][Cfg<kPair>::kBRows * BK];
+  // finished tile on its way to D: BF16 -> the two column halves in two
+  // 32 KB slots; FP32 -> one half at a time in all 64 KB
+  uint8_t out[kOutBytes];
   float sa[kScaleSlots][BM];
   float sb[kScaleSlots][BN];
-  uint8_t epi[8][32 * 64];   // per promotion warp: 32 rows x 64 B output staging
   uint64_t full[Cfg<kPair>::kStages];
-  uint64_t empty[Cfg<kPair>::kStages];
-  uint64_t tfull[2];
+  uint64_t done[Cfg<kPair>::kStages];   // MMAs of the stage complete
   uint64_t tempty[2];
   uint64_t sfull[kScaleSlots];
   uint64_t sempty[kScaleSlots];
+  uint64_t ofull[2];                     // column half h staged
+  uint64_t ofree[2];                     // its staging read out
   uint64_t final_bar;
   uint32_t tmem_base;
   volatile uint32_t abort_flag;
@@ -122,9 +148,10 @@ __device__ __forceinline__ void raise_abort(volatile uint32_t* flag) {
 template <bool kPair, bool kARow, bool kBRow, bool kBF16Out>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const float* __restrict__ sA, const float* __restrict__ sB,
-                    const float* __restrict__ Cin, void* __restrict__ Dout, int M, int N, int K,
-                    uint32_t idesc, bool vec_out, bool raster_n) {
+                    const __grid_constant__ CUtensorMap tmD, const float* __restrict__ sA,
+                    const float* __restrict__ sB, const float* __restrict__ Cin,
+                    void* __restrict__ Dout, int M, int N, int K, uint32_t idesc, bool tma_out,
+                    bool raster_n) {
   using C = Cfg<kPair>;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -144,11 +171,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
-      mbar_init(smem_u32(&sm.empty[s]), 1);
+      mbar_init(smem_u32(&sm.done[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&sm.tfull[b]), 1);
       mbar_init(smem_u32(&sm.tempty[b]), C::kPromoArrivals);
+      mbar_init(smem_u32(&sm.ofull[b]), 4);
+      mbar_init(smem_u32(&sm.ofree[b]), 1);
     }
     for (int s = 0; s < kScaleSlots; ++s) {
       mbar_init(smem_u32(&sm.sfull[s]), 32);
@@ -170,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (tma_out) tma_prefetch_desc(&tmD);
   }
   tc_fence_before();
   __syncthreads();
@@ -193,12 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (sm.abort_flag) { ok = false; break; }
         const int s = static_cast<int>(it % kStages);
         const uint32_t ph = (it / kStages) & 1u;
-        const int ss = static_cast<int>(it % kScaleSlots);
-        const uint32_t phs = (it / kScaleSlots) & 1u;
         int good = 1;
         if (lane == 0) {
-          good = mbar_wait(smem_u32(&sm.empty[s]), ph ^ 1u) &&
-                 mbar_wait(smem_u32(&sm.sempty[ss]), phs ^ 1u);
+          good = mbar_wait(smem_u32(&sm.done[s]), ph ^ 1u);
           if (good) {
             const uint32_t fb = smem_u32(&sm.full[s]);
             if (kPair) {
@@ -218,7 +244,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         good = __shfl_sync(0xffffffffu, good, 0);
         if (!good) { ok = false; break; }
-        // scales of this K tile -> scale slot ss (this CTA's rows, all 256 columns)
+      }
+    }
+    // the even CTA's full barriers also count the peer's bytes
+    if (lane == 0 && rank == 0) drain_fills(sm.full, kStages, it);
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------------------------------------- MMA
+    setmaxnreg_dec<kRegsSmall>();
+    if (lane == 0 && rank == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = unit; t < tiles && ok; t += units) {
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          if (sm.abort_flag) { ok = false; break; }
+          const uint32_t b = it & 1u;
+          const uint32_t tph = (it >> 1) & 1u;
+          const int s = static_cast<int>(it % kStages);
+          const uint32_t ph = (it / kStages) & 1u;
+          // buffer b was drained (use it-2) and stage s holds K tile `it`
+          if (!mbar_wait(smem_u32(&sm.tempty[b]), tph ^ 1u) ||
+              !mbar_wait(smem_u32(&sm.full[s]), ph)) {
+            raise_abort(&sm.abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sm.a[s]));
+          const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sm.b[s]));
+          const uint32_t d = tmem + b * BN;
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            if (kPair)
+              mma_f8f6f4_pair(d, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+            else
+              mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+          }
+          if (kPair)
+            tc_commit_pair_mc(smem_u32(&sm.done[s]), 3);
+          else
+            tc_commit(smem_u32(&sm.done[s]));
+        }
+      }
+      // every MMA this thread issued has completed once final_bar flips
+      if (kPair)
+        tc_commit_pair(smem_u32(&sm.final_bar));
+      else
+        tc_commit(smem_u32(&sm.final_bar));
+      if (!mbar_wait(smem_u32(&sm.final_bar), 0)) raise_abort(&sm.abort_flag);
+    }
+    __syncwarp();
+  } else if (warp == kScaleWarp) {
+    // ------------------------------------------------------- scale loader
+    // Each K tile's scales go to one slot of an 8-slot ring.  This warp is
+    // gated only by the promotion warps releasing slots, so it runs up to
+    // eight K tiles ahead of them and the loads' latency stays off the
+    // MMA -> drain -> MMA chain.
+    setmaxnreg_dec<kRegsSmall>();
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = unit; t < tiles && ok; t += units) {
+      const TileCoord tc = tile_coord(t, num_m, num_n, raster_n);
+      const int m_cta = tc.m * C::kTileM + static_cast<int>(rank) * BM;
+      for (int kt = 0; kt < KT; ++kt, ++it) {
+        if (sm.abort_flag) { ok = false; break; }
+        const int ss = static_cast<int>(it % kScaleSlots);
+        const uint32_t phs = (it / kScaleSlots) & 1u;
+        int good = 1;
+        if (lane == 0) {
+          good = mbar_wait(smem_u32(&sm.sempty[ss]), phs ^ 1u);
+          if (!good) raise_abort(&sm.abort_flag);
+        }
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) { ok = false; break; }
+        // this CTA's 128 rows of A, all 256 columns of the tile
         if (kARow) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -243,58 +342,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     cp_async_wait_all();
-    // the even CTA's full barriers also count the peer's bytes
-    if (lane == 0 && rank == 0) drain_fills(sm.full, kStages, it);
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ----------------------------------------------------------------- MMA
+  } else if (warp == kStoreWarp) {
+    // -------------------------------------------------------- output store
     setmaxnreg_dec<kRegsSmall>();
-    if (lane == 0 && rank == 0) {
-      uint32_t it = 0;
-      bool ok = true;
-      for (int t = unit; t < tiles && ok; t += units) {
-        for (int kt = 0; kt < KT; ++kt, ++it) {
-          if (sm.abort_flag) { ok = false; break; }
-          const uint32_t b = it & 1u;
-          const uint32_t tph = (it >> 1) & 1u;
-          const int s = static_cast<int>(it % kStages);
-          const uint32_t ph = (it / kStages) & 1u;
-          if (!mbar_wait(smem_u32(&sm.tempty[b]), tph ^ 1u) ||
-              !mbar_wait(smem_u32(&sm.full[s]), ph)) {
-            raise_abort(&sm.abort_flag);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sm.a[s]));
-          const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sm.b[s]));
-          const uint32_t d = tmem + b * BN;
-#pragma unroll
-          for (int kk = 0; kk < BK / 32; ++kk) {
-            if (kPair)
-              mma_f8f6f4_pair(d, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : 0u);
-            else
-              mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : 0u);
-          }
-          if (kPair) {
-            tc_commit_pair_mc(smem_u32(&sm.empty[s]), 3);
-            tc_commit_pair_mc(smem_u32(&sm.tfull[b]), 3);
-          } else {
-            tc_commit(smem_u32(&sm.empty[s]));
-            tc_commit(smem_u32(&sm.tfull[b]));
-          }
+    constexpr int kElem = kBF16Out ? 2 : 4;
+    constexpr int kBoxCols = 128 / kElem;              // columns of one swizzled box
+    constexpr int kHalfBlocks = 128 / kBoxCols;        // boxes of a 128-column half
+    uint32_t tl = 0;
+    bool ok = true;
+    for (int t = unit; t < tiles && ok; t += units, ++tl) {
+      const TileCoord tc = tile_coord(t, num_m, num_n, raster_n);
+      const int row0 = tc.m * C::kTileM + static_cast<int>(rank) * BM;   // this CTA's rows
+      for (int h = 0; h < 2; ++h) {
+        if (sm.abort_flag) { ok = false; break; }
+        int good = 1;
+        if (lane == 0) {
+          good = mbar_wait(smem_u32(&sm.ofull[h]), tl & 1u);
+          if (!good) raise_abort(&sm.abort_flag);
         }
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) { ok = false; break; }
+        const uint32_t base = smem_u32(sm.out) + (kBF16Out ? h * (kOutBytes / 2) : 0u);
+        const int col0 = tc.n * BN + h * 128;
+        if (tma_out) {
+          if (lane == 0) {
+            for (int blk = 0; blk < kHalfBlocks; ++blk) {
+              const int x = col0 + blk * kBoxCols;
+              if (x < N && row0 < M) tma_store_2d(&tmD, base + blk * kOutBlock, x, row0);
+            }
+            bulk_commit_group();
+            bulk_wait_group_read0();   // the staging may be overwritten from here on
+          }
+        } else {
+          // 16-byte pieces of 128 rows x 128 columns, bounds-checked
+          constexpr int kPieces = 128 * 128 * kElem / 16;
+          constexpr int kPerPiece = 16 / kElem;
+          for (int i = lane; i < kPieces; i += 32) {
+            const int r = i / (kPieces / 128);
+            const int c = i % (kPieces / 128);           // piece along the row
+            const int blk = c / 8, cc = c % 8;
+            const uint4 u = ld_shared_v4(base + blk * kOutBlock + r * 128 + ((cc ^ (r & 7)) << 4));
+            const int64_t grow = static_cast<int64_t>(row0) + r;
+            const int col = col0 + c * kPerPiece;
+            if (grow >= M || col >= N) continue;
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int j = 0; j < kPerPiece; ++j) {
+              if (col + j >= N) break;
+              if (kBF16Out)
+                reinterpret_cast<uint16_t*>(Dout)[grow * N + col + j] =
+                    static_cast<uint16_t>(w[j / 2] >> (16 * (j % 2)));
+              else
+                reinterpret_cast<float*>(Dout)[grow * N + col + j] = __uint_as_float(w[j]);
+            }
+          }
+          __syncwarp();
+        }
+        if (lane == 0) mbar_arrive(smem_u32(&sm.ofree[h]));
       }
-      // every MMA this thread issued has completed once final_bar flips
-      if (kPair)
-        tc_commit_pair(smem_u32(&sm.final_bar));
-      else
-        tc_commit(smem_u32(&sm.final_bar));
-      if (!mbar_wait(smem_u32(&sm.final_bar), 0)) raise_abort(&sm.abort_flag);
     }
+    if (tma_out && lane == 0) bulk_wait_group0();   // stores complete before the CTA exits
     __syncwarp();
-  } else if (warp < kFirstPromoWarp) {
-    setmaxnreg_dec<kRegsSmall>();            // idle warps of warpgroup 0
   } else {
     // ------------------------------------------------- promotion + epilogue
     setmaxnreg_inc<kRegsLarge>();
@@ -302,23 +411,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = (warp - kFirstPromoWarp) >> 2;   // column half of the 256-wide tile
     const int row = q * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + g * 128;
-    const uint64_t stream_out = l2_policy_evict_first();   // the result is not re-read
     // where this warp reports a drained buffer: the issuing CTA's barrier
     const uint32_t tempty0 = kPair ? mapa_shared(smem_u32(&sm.tempty[0]), 0) : smem_u32(&sm.tempty[0]);
-    uint32_t it = 0;
+    uint32_t it = 0, tl = 0;
     bool ok = true;
-    for (int t = unit; t < tiles && ok; t += units) {
+    for (int t = unit; t < tiles && ok; t += units, ++tl) {
       const TileCoord tc = tile_coord(t, num_m, num_n, raster_n);
       uint64_t acc[64];                            // 128 FP32 accumulators, in pairs
 #pragma unroll
       for (int j = 0; j < 64; ++j) acc[j] = 0ull;
       for (int kt = 0; kt < KT; ++kt, ++it) {
         const uint32_t b = it & 1u;
-        const uint32_t tph = (it >> 1) & 1u;
+        const int s = static_cast<int>(it % kStages);
+        const uint32_t ph = (it / kStages) & 1u;
         const int ss = static_cast<int>(it % kScaleSlots);
         const uint32_t phs = (it / kScaleSlots) & 1u;
+        // the MMA can run at most two K tiles ahead of this drain (two TMEM
+        // buffers), less than a round of the stage ring, so done[s] is never
+        // more than one phase past the one waited for
         if (sm.abort_flag || !mbar_wait(smem_u32(&sm.sfull[ss]), phs) ||
-            !mbar_wait(smem_u32(&sm.tfull[b]), tph)) {
+            !mbar_wait(smem_u32(&sm.done[s]), ph)) {
           if (!sm.abort_flag) raise_abort(&sm.abort_flag);
           ok = false;
           break;
@@ -328,62 +440,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sc = kBRow ? sa : sa * sm.sb[ss][g * 128];
         const uint64_t sc2 = f32x2_pack(sc, sc);
         const uint32_t taddr = lane_base + b * BN;
-        uint32_t r0[16], r1[16];
-        tmem_ld_16(taddr, r0);
-        tc_wait_ld_16(r0);
+        // kDrainCols columns per tcgen05.ld, double-buffered; the buffer is
+        // handed back to the MMA as soon as its last load has landed, before
+        // the last chunk's FMAs
+        constexpr int kChunks = 128 / kDrainCols;
+        uint32_t r0[kDrainCols], r1[kDrainCols];
+        tmem_ld_cols(taddr, r0);
+        tmem_wait_cols(r0);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t (&cur)[16] = (c & 1) ? r1 : r0;
-          uint32_t (&nxt)[16] = (c & 1) ? r0 : r1;
-          if (c + 1 < 8) tmem_ld_16(taddr + (c + 1) * 16, nxt);
+        for (int c = 0; c < kChunks; ++c) {
+          uint32_t (&cur)[kDrainCols] = (c & 1) ? r1 : r0;
+          uint32_t (&nxt)[kDrainCols] = (c & 1) ? r0 : r1;
+          if (c + 1 < kChunks) tmem_ld_cols(taddr + (c + 1) * kDrainCols, nxt);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < kDrainCols / 2; ++j) {
             const uint64_t p = f32x2_pack(__uint_as_float(cur[2 * j]), __uint_as_float(cur[2 * j + 1]));
+            const int pair_idx = (c * kDrainCols) / 2 + j;
             if (kBRow) {
-              const float2 sbv = *reinterpret_cast<const float2*>(&sm.sb[ss][g * 128 + c * 16 + 2 * j]);
-              ffma2(acc[c * 8 + j], fmul2(sc2, f32x2_pack(sbv.x, sbv.y)), p);
+              const float2 sbv = *reinterpret_cast<const float2*>(&sm.sb[ss][g * 128 + 2 * pair_idx]);
+              ffma2(acc[pair_idx], fmul2(sc2, f32x2_pack(sbv.x, sbv.y)), p);
             } else {
-              ffma2(acc[c * 8 + j], sc2, p);
+              ffma2(acc[pair_idx], sc2, p);
             }
           }
-          if (c + 1 < 8) tc_wait_ld_16(nxt);
+          if (c + 1 < kChunks) tmem_wait_cols(nxt);
+          if (c == kChunks - 2) {
+            // every tcgen05.ld of this buffer has completed: nothing to
+            // publish, so a relaxed arrive suffices
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_relaxed(tempty0 + b * 8);
+          }
         }
-        tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          // this warp's reads of the buffer and of the scale slot are complete
-          // (wait::ld returned, the scales were used): nothing to publish
-          mbar_arrive_relaxed(tempty0 + b * 8);
-          mbar_arrive_relaxed(smem_u32(&sm.sempty[ss]));
-        }
+        if (lane == 0) mbar_arrive_relaxed(smem_u32(&sm.sempty[ss]));   // scales used
       }
       if (!ok) break;
-      // ---- epilogue.  Each thread holds one row x 128 columns.  The warp
-      // passes its 32 rows through a 32 x 64-byte staging buffer (16-byte
-      // pieces XOR-swizzled by row, so both phases are bank-conflict free)
-      // and writes back 8 rows x 64 contiguous bytes per store instruction
-      // instead of 32 scattered 16-byte pieces.
-      const int64_t row0 = static_cast<int64_t>(tc.m) * C::kTileM + rank * BM + q * 32;
-      const int gcol0 = tc.n * BN + g * 128;
-      const uint32_t stage = smem_u32(sm.epi[warp - kFirstPromoWarp]);
-      constexpr int kElem = kBF16Out ? 2 : 4;
-      constexpr int kColsPerChunk = 64 / kElem;     // 32 (BF16) or 16 (FP32)
-      constexpr int kPerPiece = 16 / kElem;         // values per 16-byte piece
-      const int64_t my_row = row0 + lane;
+      // ---- epilogue: this thread's row x 128 columns go to the staging
+      // buffer as 16-byte pieces in the 128-byte-swizzled box layout (piece
+      // c of row r at r*128 + ((c ^ (r & 7)) << 4) inside its box), which
+      // the TMA store reads and which spreads a warp's 32 rows over all
+      // banks.  BF16: half g owns slot g and waits for the store of its own
+      // previous tile; FP32: a half fills the whole buffer, so half 0 waits
+      // for the previous tile's half 1 and half 1 for this tile's half 0.
+      {
+        constexpr int kElem = kBF16Out ? 2 : 4;
+        constexpr int kPerPiece = 16 / kElem;
+        const uint32_t wb = kBF16Out ? static_cast<uint32_t>(g) : static_cast<uint32_t>(g ^ 1);
+        const uint32_t wph = kBF16Out ? ((tl & 1u) ^ 1u) : (g == 0 ? ((tl & 1u) ^ 1u) : (tl & 1u));
+        if (!mbar_wait(smem_u32(&sm.ofree[wb]), wph)) {
+          raise_abort(&sm.abort_flag);
+          break;
+        }
+        const uint32_t base = smem_u32(sm.out) + (kBF16Out ? g * (kOutBytes / 2) : 0u);
+        const int64_t grow = static_cast<int64_t>(tc.m) * C::kTileM + rank * BM + row;
+        const int gcol0 = tc.n * BN + g * 128;
 #pragma unroll
-      for (int ch = 0; ch < 128 / kColsPerChunk; ++ch) {
-        const int col0 = gcol0 + ch * kColsPerChunk;
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
+        for (int c = 0; c < 128 / kPerPiece; ++c) {
           float v[kPerPiece];
 #pragma unroll
           for (int j = 0; j < kPerPiece / 2; ++j)
-            f32x2_unpack(acc[(ch * kColsPerChunk + p * kPerPiece) / 2 + j], v[2 * j], v[2 * j + 1]);
-          if (Cin != nullptr && my_row < M) {
+            f32x2_unpack(acc[(c * kPerPiece) / 2 + j], v[2 * j], v[2 * j + 1]);
+          if (Cin != nullptr && grow < M) {
 #pragma unroll
             for (int j = 0; j < kPerPiece; ++j) {
-              const int col = col0 + p * kPerPiece + j;
-              if (col < N) v[j] += __ldg(Cin + my_row * N + col);
+              const int col = gcol0 + c * kPerPiece + j;
+              if (col < N) v[j] += __ldg(Cin + grow * N + col);
             }
           }
           uint4 u;
@@ -396,35 +518,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             u = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
                            __float_as_uint(v[2 % kPerPiece]), __float_as_uint(v[3 % kPerPiece]));
           }
-          st_shared_v4(stage + lane * 64 + ((p ^ ((lane >> 1) & 3)) << 4), u);
+          const int blk = c / 8, cc = c % 8;
+          st_shared_v4(base + blk * kOutBlock + row * 128 + ((cc ^ (row & 7)) << 4), u);
         }
+        fence_proxy_async_smem();    // the staged bytes are read by the TMA (async proxy)
         __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = 8 * i + (lane >> 2);
-          const int p = lane & 3;
-          const uint4 u = ld_shared_v4(stage + r * 64 + ((p ^ ((r >> 1) & 3)) << 4));
-          const int64_t grow = row0 + r;
-          const int col = col0 + p * kPerPiece;
-          if (grow < M && col < N) {
-            if (vec_out && col + kPerPiece <= N) {
-              st_global_v4_hint(static_cast<uint8_t*>(Dout) + (grow * N + col) * kElem, u, stream_out);
-            } else {
-              const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-              for (int j = 0; j < kPerPiece; ++j) {
-                if (col + j >= N) break;
-                if (kBF16Out) {
-                  const uint16_t h = static_cast<uint16_t>(w[j / 2] >> (16 * (j % 2)));
-                  reinterpret_cast<uint16_t*>(Dout)[grow * N + col + j] = h;
-                } else {
-                  reinterpret_cast<float*>(Dout)[grow * N + col + j] = __uint_as_float(w[j]);
-                }
-              }
-            }
-          }
-        }
-        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.ofull[g]));
       }
     }
   }
@@ -484,14 +583,15 @@ cudaError_t launch_variant(const Fp8GemmArgs& a, int num_sms, cudaStream_t s) {
   const int grid = per * (tiles < max_units ? tiles : max_units);
   const uint32_t idesc = idesc_f8f6f4(static_cast<uint32_t>(a.afmt), static_cast<uint32_t>(a.bfmt),
                                       tile_m, BN);
-  const bool vec_out = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) &&
-                       (a.out_bf16 ? (a.N % 8 == 0) : (a.N % 4 == 0));
+  // TMA stores need a 16-byte aligned D whose row pitch is a multiple of 16
+  // bytes; otherwise the store warp copies the staged tile out itself
+  const bool tma_out = a.tma_out;
   // keep the smaller operand resident: sweep it inside groups of the larger
   const bool raster_n = static_cast<int64_t>(a.M) < static_cast<int64_t>(a.N);
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.sA, a.sB, a.C, a.D, a.M, a.N, a.K, idesc,
-                            vec_out, raster_n);
+  return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmD, a.sA, a.sB, a.C, a.D, a.M, a.N, a.K,
+                            idesc, tma_out, raster_n);
 }
 
 template <bool kPair>

@@ -14,6 +14,7 @@ namespace bsg {
 cudaError_t quantize_error_read_and_clear(cudaStream_t s, uint32_t* out);
 cudaError_t gemm_fp8_error_read_and_clear(cudaStream_t s, uint32_t* out);
 cudaError_t gemm_mxfp4_error_read_and_clear(cudaStream_t s, uint32_t* out);
+cudaError_t mma_peak_error_read_and_clear(cudaStream_t s, uint32_t* out);
 
 // ------------------------------------------------------------- quantisers
 // src_bf16: source is BF16 (else FP32).  fmt: 0 E4M3, 1 E5M2.
@@ -36,6 +37,10 @@ cudaError_t launch_sf_to_tcgen05(const uint8_t* sf, int64_t rows, int64_t kblock
 // boxes of box_rows x 128 bytes with 128-byte swizzling; out of range = 0.
 bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
                      uint64_t pitch, uint32_t box_rows);
+// 2-D map of a row-major output matrix (rows x cols elements of elem_bytes,
+// 2 or 4) stored in boxes of 128 rows x 128 bytes with 128-byte swizzling.
+// Needs a 16-byte aligned base and a row pitch that is a multiple of 16 bytes.
+bool make_out_map(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols, int elem_bytes);
 // 3-D view [chunk][row][128 B] of the same matrix (inner_bytes % 128 == 0):
 // one box brings box_chunks consecutive 128-byte chunks of box_rows rows and
 // lands as box_chunks canonical (box_rows x 128 B, swizzled) slabs.
@@ -55,7 +60,9 @@ struct Fp8GemmArgs {
   void* D;
   bool out_bf16;
   bool pair;                 // CTA-pair kernel (256 x 256 tiles, tcgen05 cta_group::2)
+  bool tma_out;              // tmD is valid: D is written by TMA tensor stores
   CUtensorMap tmA, tmB;      // K-major operand maps (box 128 B x rows)
+  CUtensorMap tmD;           // output map (box 128 B x 128 rows, 128-byte swizzle)
 };
 // Whether a problem takes the CTA-pair kernel, and the B box height it needs.
 bool gemm_fp8_use_pair(int M, int N, int num_sms);
@@ -80,5 +87,11 @@ cudaError_t launch_gemm_mxfp4(const Mxfp4GemmArgs& a, int num_sms, cudaStream_t 
 // Decode-shaped (small M) MXFP4 GEMM: weights B stream once; A has M <= 32 rows.
 size_t gemm_mxfp4_decode_workspace(int M, int N, int K, int num_sms);
 cudaError_t launch_gemm_mxfp4_decode(const Mxfp4GemmArgs& a, int num_sms, cudaStream_t s);
+
+// ------------------------------------------------- tensor-core microbenchmark
+// Back-to-back tcgen05.mma from shared memory on every SM; *flops receives
+// the floating-point operations the launch performs.
+cudaError_t launch_mma_peak(bool fp4, bool pair, int64_t iters, int num_sms, cudaStream_t s,
+                            int64_t* flops);
 
 }  // namespace bsg

@@ -205,6 +205,23 @@ bsg_status bsg_gemm_decode_noalloc(int64_t M, int64_t N, int64_t K, const void* 
                                    const void* B, const void* sB, const float* C, void* D,
                                    bsg_dtype out, void* stream);
 
+/* bsg_mma_peak - tensor-core throughput microbenchmark (measurement only).
+ *
+ * No page gives GB300's FP8 or FP4 tensor rate, and no copy or library GEMM
+ * measures it, so the roofline of the GEMMs above needs a measured ceiling.
+ * One launch keeps every SM's tensor core busy with `iters` x 4 back-to-back
+ * MMAs whose operands sit in shared memory (zero-filled; no global memory
+ * traffic, no epilogue; results discarded):
+ *   fmt = BSG_E4M3: tcgen05.mma kind::f8f6f4, E4M3 x E4M3, M128 N256 K32;
+ *   fmt = BSG_E2M1: tcgen05.mma kind::mxf4.block_scale, M128 N256 K64.
+ * pair != 0 runs CTA pairs (cta_group::2, M256 per instruction).
+ * *flops (host) receives the floating-point operations of the launch
+ * (2*M*N*K per MMA); divide by the launch's duration, timed by the caller
+ * with events on `stream`.
+ * Errors: BSG_ERR_INVALID_ARG (null flops, iters <= 0 or > 2^20),
+ *         BSG_ERR_UNSUPPORTED (other formats), BSG_ERR_CUDA. */
+bsg_status bsg_mma_peak(bsg_format fmt, int pair, int64_t iters, int64_t* flops, void* stream);
+
 /* Human-readable name of a status. */
 const char* bsg_status_string(bsg_status status);
 

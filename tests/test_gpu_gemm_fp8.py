@@ -77,3 +77,21 @@ def test_fp8_pair_path_e5m2_fp32():
     A, B = synth.make("dgrad", m=M, n=N, k=K)
     rows = np.r_[0:4, 126:130, 254:258, 2556:2560]
     report("pair e5m2", *_run(A, B, "e5m2", "e4m3", "tile", "tile", "f32", rows=rows))
+
+
+@pytest.mark.parametrize("M,N,K,out", [(200, 300, 272, "bf16"), (129, 257, 16, "bf16"),
+                                       (130, 1001, 384, "f32")])
+def test_fp8_output_pitch_not_16_bytes(M, N, K, out):
+    # D's row pitch is not a multiple of 16 bytes: no TMA store; the staged
+    # tile is copied out with bounds checks
+    A, B = synth.make("ffn_up", m=M, n=N, k=K)
+    C = synth.addend("ffn_up", M, N)
+    report(f"pitch {M}x{N}x{K} {out}", *_run(A, B, "e4m3", "e4m3", "row", "tile", out, C=C))
+
+
+@pytest.mark.parametrize("N,out", [(2004, "bf16"), (2001, "f32")])
+def test_fp8_pair_path_output_pitch_not_16_bytes(N, out):
+    M, K = 4100, 256
+    A, B = synth.make("ffn_up", m=M, n=N, k=K)
+    rows = np.array([0, 127, 128, 255, 256, 2047, 2048, 4095, 4096, 4099])
+    report(f"pair pitch N={N} {out}", *_run(A, B, "e4m3", "e4m3", "row", "tile", out, rows=rows))
