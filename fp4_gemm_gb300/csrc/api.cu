@@ -158,6 +158,7 @@ bsg_status bsg_quantize_fp8(const void* x, bsg_dtype src, int64_t rows, int64_t 
   if (gran != BSG_SCALE_TILE128x128 && gran != BSG_SCALE_ROW1x128) return BSG_ERR_UNSUPPORTED;
   if (!aligned(x, src == BSG_F32 ? 4 : 2) || !aligned(scales, 4)) return BSG_ERR_ALIGNMENT;
   if (gran == BSG_SCALE_TILE128x128 && cdiv(rows, 128) > 65535) return BSG_ERR_INVALID_ARG;
+  if (gran == BSG_SCALE_ROW1x128 && cdiv(cdiv(cols, 128), 4) > 65535) return BSG_ERR_INVALID_ARG;
   const float fm = fmt_max == 0.0f ? (fmt == BSG_E4M3 ? 448.0f : 57344.0f) : fmt_max;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int f = fmt == BSG_E4M3 ? 0 : 1;

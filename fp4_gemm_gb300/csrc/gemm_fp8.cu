@@ -349,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kElem = kBF16Out ? 2 : 4;
     constexpr int kBoxCols = 128 / kElem;              // columns of one swizzled box
     constexpr int kHalfBlocks = 128 / kBoxCols;        // boxes of a 128-column half
+    const uint64_t stream_out = l2_policy_evict_first();   // D is not re-read here
     uint32_t tl = 0;
     bool ok = true;
     for (int t = unit; t < tiles && ok; t += units, ++tl) {
@@ -369,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             for (int blk = 0; blk < kHalfBlocks; ++blk) {
               const int x = col0 + blk * kBoxCols;
-              if (x < N && row0 < M) tma_store_2d(&tmD, base + blk * kOutBlock, x, row0);
+              if (x < N && row0 < M) tma_store_2d_hint(&tmD, base + blk * kOutBlock, x, row0, stream_out);
             }
             bulk_commit_group();
             bulk_wait_group_read0();   // the staging may be overwritten from here on

@@ -116,26 +116,31 @@ __device__ __forceinline__ void store_codes4(uint8_t* q, int64_t off, int64_t co
   }
 }
 
-// One CTA per 128 x 128 tile; 256 threads, thread t owns columns 4*(t%32)..+3
-// of rows t/32 + 8i, i < 16.
+// One CTA per 128 x 128 tile; 512 threads, thread t owns columns 4*(t%32)..+3
+// of rows t/32 + 16i, i < 8 (32 values in registers, so several CTAs fit on
+// an SM and keep enough loads in flight).
+constexpr int kTileThreads = 512;
+constexpr int kTileRowsPerThread = 128 / (kTileThreads / 32);
+
 template <bool kBF16>
-__global__ void __launch_bounds__(256) quantize_fp8_tile_kernel(
+__global__ void __launch_bounds__(kTileThreads) quantize_fp8_tile_kernel(
     const void* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, int fmt, float fmt_max,
     bool vec_in, bool vec_out, uint8_t* __restrict__ q, float* __restrict__ scales) {
   grid_dep_launch();
   grid_dep_wait();
-  __shared__ float warp_max[8];
+  constexpr int kWarps = kTileThreads / 32;
+  __shared__ float warp_max[kWarps];
   __shared__ float tile_scale;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
   const int cg = threadIdx.x & 31;
   const int rr = threadIdx.x >> 5;
   const int64_t col = c0 + 4 * cg;
-  float v[16][4];
+  float v[kTileRowsPerThread][4];
   float amax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int64_t row = r0 + rr + 8 * i;
+  for (int i = 0; i < kTileRowsPerThread; ++i) {
+    const int64_t row = r0 + rr + kWarps * i;
     if (row < rows && col < cols) {
       load4<kBF16>(x, row, col, cols, ld, vec_in, v[i]);
     } else {
@@ -151,7 +156,7 @@ __global__ void __launch_bounds__(256) quantize_fp8_tile_kernel(
   if (threadIdx.x == 0) {
     float m = warp_max[0];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) m = fmaxf(m, warp_max[w]);
+    for (int w = 1; w < kWarps; ++w) m = fmaxf(m, warp_max[w]);
     const float s = fp8_scale(m, fmt_max);
     tile_scale = s;
     scales[static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x] = s;
@@ -159,8 +164,8 @@ __global__ void __launch_bounds__(256) quantize_fp8_tile_kernel(
   __syncthreads();
   const GroupDiv div(tile_scale);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int64_t row = r0 + rr + 8 * i;
+  for (int i = 0; i < kTileRowsPerThread; ++i) {
+    const int64_t row = r0 + rr + kWarps * i;
     if (row < rows && col < cols) {
       const uint32_t c = cvt4_fp8(fmt, div(v[i][0]), div(v[i][1]), div(v[i][2]), div(v[i][3]));
       store_codes4(q, row * cols + col, col, cols, vec_out, c);
@@ -168,40 +173,42 @@ __global__ void __launch_bounds__(256) quantize_fp8_tile_kernel(
   }
 }
 
-// One warp per (row, 128-wide K tile); each warp takes 4 consecutive items.
-// Scales stored K-tile major: scales[t * rows + row].
+// Block (8 rows) x (4 K tiles of 128): warp w takes row 8*blockIdx.x + w and
+// K tiles 4*blockIdx.y .. +3, lane l columns 4l..4l+3 of each.  Scales are
+// stored K-tile major, scales[t * rows + row], so a block's eight rows of one
+// K tile fill one 32-byte sector.
+constexpr int kRowWarps = 8;
+constexpr int kRowTiles = 4;
+
 template <bool kBF16>
-__global__ void __launch_bounds__(256) quantize_fp8_row_kernel(
+__global__ void __launch_bounds__(kRowWarps * 32) quantize_fp8_row_kernel(
     const void* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, int fmt, float fmt_max,
     bool vec_in, bool vec_out, uint8_t* __restrict__ q, float* __restrict__ scales) {
   grid_dep_launch();
   grid_dep_wait();
-  constexpr int kItems = 4;
   const int64_t kt = (cols + 127) / 128;
-  const int64_t total = rows * kt;
-  const int64_t first = (static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * kItems;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
+  const int64_t t0 = static_cast<int64_t>(blockIdx.y) * kRowTiles;
   const int lane = threadIdx.x & 31;
-  float v[kItems][4];
+  if (row >= rows) return;   // uniform across the warp
+  float v[kRowTiles][4];
 #pragma unroll
-  for (int i = 0; i < kItems; ++i) {
-    const int64_t it = first + i;
-    const int64_t row = it / kt, t = it % kt;
-    const int64_t col = t * 128 + 4 * lane;
-    if (it < total && col < cols) {
+  for (int i = 0; i < kRowTiles; ++i) {
+    const int64_t col = (t0 + i) * 128 + 4 * lane;
+    if (t0 + i < kt && col < cols) {
       load4<kBF16>(x, row, col, cols, ld, vec_in, v[i]);
     } else {
       v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.0f;
     }
   }
 #pragma unroll
-  for (int i = 0; i < kItems; ++i) {
-    const int64_t it = first + i;
-    if (it >= total) break;  // uniform across the warp
+  for (int i = 0; i < kRowTiles; ++i) {
+    const int64_t t = t0 + i;
+    if (t >= kt) break;  // uniform across the warp
     float amax = fmaxf(fmaxf(fabsf(v[i][0]), fabsf(v[i][1])), fmaxf(fabsf(v[i][2]), fabsf(v[i][3])));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float s = fp8_scale(amax, fmt_max);
-    const int64_t row = it / kt, t = it % kt;
     const int64_t col = t * 128 + 4 * lane;
     if (lane == 0) scales[t * rows + row] = s;
     if (col < cols) {
@@ -331,8 +338,8 @@ cudaError_t launch_quantize_fp8_tile(const void* x, bool src_bf16, int64_t rows,
   const bool vec_out = aligned(q, 4) && cols % 4 == 0;
   dim3 grid(static_cast<unsigned>((cols + 127) / 128), static_cast<unsigned>((rows + 127) / 128));
   auto kern = src_bf16 ? quantize_fp8_tile_kernel<true> : quantize_fp8_tile_kernel<false>;
-  return launch_pdl(kern, grid, dim3(256), 0, s, x, rows, cols, ld, fmt, fmt_max, vec_in, vec_out,
-                    q, scales);
+  return launch_pdl(kern, grid, dim3(kTileThreads), 0, s, x, rows, cols, ld, fmt, fmt_max, vec_in,
+                    vec_out, q, scales);
 }
 
 cudaError_t launch_quantize_fp8_row(const void* x, bool src_bf16, int64_t rows, int64_t cols,
@@ -340,11 +347,12 @@ cudaError_t launch_quantize_fp8_row(const void* x, bool src_bf16, int64_t rows, 
                                     cudaStream_t s) {
   const bool vec_in = src_bf16 ? (aligned(x, 8) && ld % 4 == 0) : (aligned(x, 16) && ld % 4 == 0);
   const bool vec_out = aligned(q, 4) && cols % 4 == 0;
-  const int64_t items = rows * ((cols + 127) / 128);
-  const int64_t blocks = (items + 31) / 32;  // 8 warps x 4 items
+  const int64_t kt = (cols + 127) / 128;
+  const dim3 grid(static_cast<unsigned>((rows + kRowWarps - 1) / kRowWarps),
+                  static_cast<unsigned>((kt + kRowTiles - 1) / kRowTiles));
   auto kern = src_bf16 ? quantize_fp8_row_kernel<true> : quantize_fp8_row_kernel<false>;
-  return launch_pdl(kern, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, x, rows, cols, ld,
-                    fmt, fmt_max, vec_in, vec_out, q, scales);
+  return launch_pdl(kern, grid, dim3(kRowWarps * 32), 0, s, x, rows, cols, ld, fmt, fmt_max,
+                    vec_in, vec_out, q, scales);
 }
 
 cudaError_t launch_quantize_mxfp4(const void* x, bool src_bf16, int64_t rows, int64_t cols,

@@ -106,7 +106,9 @@ typedef enum {
  *          maximum (448 for E4M3, 57344 for E5M2).  Must be >= 0 and finite.
  * q        device, rows x cols codes, leading dimension `cols` bytes.
  * scales   device, FP32 scales in the layout `gran` describes.
- * Errors: BSG_ERR_INVALID_ARG (null, rows/cols <= 0, ld < cols, bad fmt_max),
+ * Errors: BSG_ERR_INVALID_ARG (null, rows/cols <= 0, ld < cols, bad fmt_max,
+ *         more than 65535 * 128 rows for 128 x 128 scales or more than
+ *         65535 * 512 columns for 1 x 128 scales),
  *         BSG_ERR_UNSUPPORTED (fmt or gran not FP8), BSG_ERR_CUDA.
  */
 bsg_status bsg_quantize_fp8(const void* x, bsg_dtype src, int64_t rows, int64_t cols,
