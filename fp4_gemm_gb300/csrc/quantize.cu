@@ -96,6 +96,10 @@ struct GroupDiv {
     fast = s_ >= 0x1p-80f && s_ <= 0x1p80f;
     r = __frcp_rn(s_);
   }
+  // r_ must be RN(1 / s_), computed once for the group and shared
+  __device__ __forceinline__ GroupDiv(float s_, float r_) : s(s_), r(r_) {
+    fast = s_ >= 0x1p-80f && s_ <= 0x1p80f;
+  }
   __device__ __forceinline__ float operator()(float x) const {
     if (!fast) return __fdiv_rn(x, s);
     const float q0 = x * r;
@@ -130,7 +134,7 @@ __global__ void __launch_bounds__(kTileThreads) quantize_fp8_tile_kernel(
   grid_dep_wait();
   constexpr int kWarps = kTileThreads / 32;
   __shared__ float warp_max[kWarps];
-  __shared__ float tile_scale;
+  __shared__ float tile_scale, tile_rcp;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
   const int cg = threadIdx.x & 31;
@@ -159,10 +163,11 @@ __global__ void __launch_bounds__(kTileThreads) quantize_fp8_tile_kernel(
     for (int w = 1; w < kWarps; ++w) m = fmaxf(m, warp_max[w]);
     const float s = fp8_scale(m, fmt_max);
     tile_scale = s;
+    tile_rcp = __frcp_rn(s);
     scales[static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x] = s;
   }
   __syncthreads();
-  const GroupDiv div(tile_scale);
+  const GroupDiv div(tile_scale, tile_rcp);
 #pragma unroll
   for (int i = 0; i < kTileRowsPerThread; ++i) {
     const int64_t row = r0 + rr + kWarps * i;
@@ -201,18 +206,32 @@ __global__ void __launch_bounds__(kRowWarps * 32) quantize_fp8_row_kernel(
       v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.0f;
     }
   }
+  // group maxima (every lane ends with all four), then lane i computes the
+  // scale and its reciprocal of group i - the correctly rounded divisions
+  // run once per group instead of once per lane - and broadcasts them
+  float am[kRowTiles];
+#pragma unroll
+  for (int i = 0; i < kRowTiles; ++i) {
+    float a = fmaxf(fmaxf(fabsf(v[i][0]), fabsf(v[i][1])), fmaxf(fabsf(v[i][2]), fabsf(v[i][3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    am[i] = a;
+  }
+  float mine = am[0];
+#pragma unroll
+  for (int i = 1; i < kRowTiles; ++i) mine = lane == i ? am[i] : mine;
+  const float my_s = fp8_scale(mine, fmt_max);
+  const float my_r = __frcp_rn(my_s);
 #pragma unroll
   for (int i = 0; i < kRowTiles; ++i) {
     const int64_t t = t0 + i;
     if (t >= kt) break;  // uniform across the warp
-    float amax = fmaxf(fmaxf(fabsf(v[i][0]), fabsf(v[i][1])), fmaxf(fabsf(v[i][2]), fabsf(v[i][3])));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float s = fp8_scale(amax, fmt_max);
+    const float s = __shfl_sync(0xffffffffu, my_s, i);
+    const float r = __shfl_sync(0xffffffffu, my_r, i);
     const int64_t col = t * 128 + 4 * lane;
     if (lane == 0) scales[t * rows + row] = s;
     if (col < cols) {
-      const GroupDiv div(s);
+      const GroupDiv div(s, r);
       const uint32_t c = cvt4_fp8(fmt, div(v[i][0]), div(v[i][1]), div(v[i][2]), div(v[i][3]));
       store_codes4(q, row * cols + col, col, cols, vec_out, c);
     }

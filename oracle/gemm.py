@@ -12,6 +12,8 @@ fields and the scales applied per K block:
   (relative error ~1e-16, far below the comparison tolerance).
 * MXFP4 ("Rubin FP4 GEMM deep dive", §2.2 and §3.1): every element is an E2M1
   value times an E8M0 power of two, exact in FP64; D = (s_A a)(s_B b)^T + C.
+* MXFP8 (the same K-blocked rule with FP8 E4M3 / E5M2 elements): every
+  element is an FP8 value times an E8M0 power of two, exact in FP64.
 
 Both also return the per-element bound  Bnd_ij = sum_k |s_A a_k s_B b_k|,
 used by the tolerance |D_gpu - D| <= 1e-4 * Bnd + 1e-6.
@@ -83,6 +85,34 @@ def gemm_mxfp4(A: np.ndarray, sfA: np.ndarray, B: np.ndarray, sfB: np.ndarray,
     ri = np.arange(M) if rows is None else np.asarray(rows)
     a = mxfp4_values(A[ri], sfA[ri])
     b = mxfp4_values(B, sfB)
+    D = a @ b.T
+    Bnd = np.abs(a) @ np.abs(b).T
+    if C is not None:
+        D += np.asarray(C, dtype=np.float64)[ri]
+    return D, Bnd
+
+
+def mx_values(codes: np.ndarray, fmt: str, sf: np.ndarray) -> np.ndarray:
+    """Real values s * a of an MX matrix (rows x K): FP8 codes one per byte
+    (fmt "e4m3" / "e5m2") or packed E2M1 (fmt "e2m1"), with row-major E8M0
+    scales (rows x K/32), exact in FP64."""
+    if fmt == "e2m1":
+        return mxfp4_values(codes, sf)
+    vals = formats.decode_array(codes, fmt)
+    scale = formats.decode_e8m0_array(sf)
+    R, K = vals.shape
+    return (vals.reshape(R, K // 32, 32) * scale[:, :, None]).reshape(R, K)
+
+
+def gemm_mxfp8(A: np.ndarray, fa: str, sfA: np.ndarray, B: np.ndarray, fb: str, sfB: np.ndarray,
+               C: np.ndarray | None = None, rows=None):
+    """MXFP8 GEMM. A: FP8 codes M x K (format fa), sfA M x K/32; B: FP8 codes
+    N x K (format fb), sfB N x K/32 (scales row-major).  Returns (D, Bnd) in
+    FP64."""
+    M = A.shape[0]
+    ri = np.arange(M) if rows is None else np.asarray(rows)
+    a = mx_values(A[ri], fa, sfA[ri])
+    b = mx_values(B, fb, sfB)
     D = a @ b.T
     Bnd = np.abs(a) @ np.abs(b).T
     if C is not None:

@@ -143,3 +143,41 @@ def test_tolerance_helper():
     assert not ok
     ok, _ = gemm.within_tolerance(ref * (1 + 7e-3), ref, bnd, bf16=True)
     assert ok
+
+
+@pytest.mark.parametrize("fa,fb", [("e4m3", "e4m3"), ("e5m2", "e4m3")])
+def test_mxfp8_brute_force_tiny(fa, fb):
+    g = np.random.default_rng(7)
+    M, N, K = 3, 4, 96
+    xa = (g.standard_normal((M, K)) * np.exp2(g.uniform(-8, 8, (M, 1)))).astype(np.float32)
+    xb = (g.standard_normal((N, K)) * np.exp2(g.uniform(-8, 8, (N, 1)))).astype(np.float32)
+    A, sfA = quantize.quantize_mxfp8(xa, fa)
+    B, sfB = quantize.quantize_mxfp8(xb, fb)
+    C = g.standard_normal((M, N)).astype(np.float32)
+    D, Bnd = gemm.gemm_mxfp8(A, fa, sfA, B, fb, sfB, C=C)
+    dec = {"e4m3": formats.decode_e4m3, "e5m2": formats.decode_e5m2}
+    for i in range(M):
+        for j in range(N):
+            acc = Fraction(float(C[i, j]))
+            bnd = Fraction(0)
+            for k in range(K):
+                ta = Fraction(dec[fa](int(A[i, k]))) * Fraction(2) ** (int(sfA[i, k // 32]) - 127)
+                tb = Fraction(dec[fb](int(B[j, k]))) * Fraction(2) ** (int(sfB[j, k // 32]) - 127)
+                acc += ta * tb
+                bnd += abs(ta * tb)
+            assert abs(D[i, j] - float(acc)) <= 1e-15 * float(bnd) + 1e-300
+            assert Bnd[i, j] == pytest.approx(float(bnd), rel=1e-15)
+
+
+def test_mxfp8_all_ones_closed_form_with_scales():
+    # every element 1.0 (E4M3 0x38), A's scales 2^1 on its first K block and
+    # 2^0 elsewhere, B's scales 2^-3: D = K/32 blocks * 32 * 2^(eA - 3)
+    M, N, K = 2, 3, 128
+    A = np.full((M, K), 0x38, np.uint8)
+    B = np.full((N, K), 0x38, np.uint8)
+    sfA = np.full((M, K // 32), 127, np.uint8)
+    sfA[:, 0] = 128
+    sfB = np.full((N, K // 32), 124, np.uint8)
+    D, Bnd = gemm.gemm_mxfp8(A, "e4m3", sfA, B, "e4m3", sfB)
+    expect = (32 * 2.0 + 3 * 32 * 1.0) * 2.0 ** -3
+    assert np.all(D == expect) and np.all(Bnd == expect)

@@ -134,3 +134,67 @@ def test_tcgen05_layout_is_a_permutation():
     assert out.size == 2 * 3 * 512
     # each source byte lands in exactly one place and the rest is padding (127)
     assert sorted(out.tolist()) == sorted(sf.ravel().tolist() + [127] * (out.size - sf.size))
+
+
+def test_mxfp8_hand_worked_e4m3():
+    # E4M3 max 448.  Block max 448 -> v = 1 -> 2^0; 672 -> v = 1.5 -> tie -> 2^1;
+    # 600 -> v = 1.34 -> 2^0 (600 saturates to 448); 0 -> code 127.
+    x = np.zeros((4, 32), np.float32)
+    x[0, :3] = [448.0, -1.0, 0.3]
+    x[1, :3] = [672.0, -336.0, 2.0]
+    x[2, :2] = [600.0, 17.0]
+    codes, sf = quantize.quantize_mxfp8(x, "e4m3")
+    assert list(sf[:, 0]) == [127, 128, 127, 127]
+    vals = formats.decode_array(codes, "e4m3")
+    assert list(vals[0, :3]) == [448.0, -1.0, 0.3125]        # 0.3 -> 0.3125 (1.25 * 2^-2)
+    # after dividing by 2: 336 is half way between 320 and 352 and -168 half
+    # way between -160 and -176; both go to the even mantissa
+    assert list(vals[1, :3]) == [320.0, -160.0, 1.0]
+    # 17 is half way between 16 and 18: even mantissa -> 16
+    assert list(vals[2, :2]) == [448.0, 16.0]
+    assert (vals[3] == 0).all()
+
+
+def test_mxfp8_hand_worked_e5m2_and_fmt_max():
+    # E5M2 max 57344: block max 57344 -> 2^0; 3 * 57344 / 2 = 86016 -> tie -> 2^1
+    x = np.zeros((2, 32), np.float32)
+    x[0, :2] = [57344.0, 3.0]
+    x[1, :2] = [86016.0, -5.0]
+    packed, sf = quantize.quantize_mxfp8(x, "e5m2")
+    assert list(sf[:, 0]) == [127, 128]
+    vals = formats.decode_array(packed, "e5m2")
+    assert list(vals[0, :2]) == [57344.0, 3.0]
+    assert list(vals[1, :2]) == [40960.0, -2.5]              # 43008 -> 40960 (tie to even), -2.5 exact
+    # fmt_max = 448 for E5M2 maps the block maximum to 448 instead
+    _, sf448 = quantize.quantize_mxfp8(x, "e5m2", fmt_max=448.0)
+    assert list(sf448[:, 0]) == [127 + 7, 127 + 8]           # 57344 / 448 = 128 = 2^7; 86016/448 = 192 -> 2^8 (tie up)
+
+
+def test_mxfp8_reconstruction_bound():
+    # each element is within half an FP8 step (times the scale) of its source,
+    # or clipped at fmt_max * scale; scaled block maxima stay below 1.5 * fmt_max
+    g = np.random.default_rng(6)
+    x = (g.standard_normal((64, 256)) * np.exp2(g.uniform(-12, 12, (64, 1)))).astype(np.float32)
+    for fmt, mant in (("e4m3", 3), ("e5m2", 2)):
+        codes, sf = quantize.quantize_mxfp8(x, fmt)
+        fm = formats.max_finite(fmt)
+        vals = formats.decode_array(codes, fmt)
+        scale = np.repeat(np.ldexp(1.0, sf.astype(np.int64) - 127), 32, axis=1)
+        y = x.astype(np.float64) / scale
+        assert np.all(np.abs(y).reshape(64, 8, 32).max(axis=2) <= 1.5 * fm)
+        clipped = np.abs(y) > fm
+        assert np.all(np.abs(vals[clipped]) == fm)
+        # spacing of the format at |y| (normal range), never below the subnormal step
+        emin = -6 if fmt == "e4m3" else -14
+        e = np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** emin)))
+        step = np.exp2(e - mant)
+        assert np.all(np.abs(vals - y)[~clipped] <= step[~clipped] / 2)
+
+
+def test_mxfp8_zero_block_and_sizes():
+    K = 4096
+    x = np.zeros((2, K), np.float32)
+    x[1, 100] = 3.0
+    codes, sf = quantize.quantize_mxfp8(x, "e4m3")
+    assert codes.shape == (2, K) and sf.shape == (2, K // int(FACTS["mx_block"]))
+    assert (sf[0] == 127).all() and (codes[0] == 0).all()
