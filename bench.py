@@ -14,6 +14,10 @@ Workloads (synthetic, seeded; see synth/):
               pre-quantised MXFP4 weights, BF16 out.  Metric GB/s of algorithmic
               bytes (weights + scales + activations + output).
   fp8_256, mxfp4_1024   the small parity configurations (latency-bound).
+  mxfp8_ffn_up  the FFN-up shape and inputs with MXFP8 operands (E4M3, one
+              E8M0 scale per 32 along K, applied by the tensor core, so the
+              GEMM needs no promotion): quantise the activations with the MX
+              rule, then the block-scaled FP8 GEMM, BF16 out.
 
 One JSON line is printed by rank 0.  Timing: W warm-up steps, then K steps.
 For the three full-size workloads every input and output exists in several
@@ -57,7 +61,10 @@ L2_BYTES = 129 << 20
 
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = {"fp8": ["gemm_fp8.cu", "common.cuh"], "fp4": ["gemm_mxfp4.cu", "common.cuh"]}
+KERNEL_SOURCES = {"fp8": ["gemm_fp8.cu", "common.cuh"], "fp4": ["gemm_mxfp4.cu", "common.cuh"],
+                  "mx8": ["gemm_mx.cu", "common.cuh"]}
+# workloads that reuse another workload's shape and seeded inputs
+SHAPE_OF = {"mxfp8_ffn_up": "ffn_up"}
 
 
 def kernel_source_hash(files):
@@ -97,7 +104,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="ffn_up",
-                    choices=["ffn_up", "dgrad", "decode", "fp8_256", "mxfp4_1024"])
+                    choices=["ffn_up", "dgrad", "decode", "fp8_256", "mxfp4_1024", "mxfp8_ffn_up"])
     ap.add_argument("--m", type=int, default=None, help="override M (e.g. 1 for decode)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -113,12 +120,14 @@ class Workload:
         import torch
         import fp4_gemm_gb300 as bsg
         self.bsg, self.torch, self.dev, self.name = bsg, torch, dev, name
-        idx, M, N, K = synth.WORKLOADS[name]
+        src = SHAPE_OF.get(name, name)
+        idx, M, N, K = synth.WORKLOADS[src]
         if m_override is not None:
             M = m_override
         self.M, self.N, self.K = M, N, K
-        A, B = synth.make(name, m=M)
+        A, B = synth.make(src, m=M)
         self.fp4 = name in ("decode", "mxfp4_1024")
+        self.mx8 = name == "mxfp8_ffn_up"
         if name == "ffn_up":
             self.fa, self.fb, self.ga, self.gb, self.out = "e4m3", "e4m3", "row", "tile", "bf16"
         elif name == "dgrad":
@@ -127,6 +136,8 @@ class Workload:
             self.fa, self.fb, self.ga, self.gb, self.out = "e4m3", "e4m3", "tile", "tile", "f32"
         elif name == "mxfp4_1024":
             self.fa, self.fb, self.ga, self.gb, self.out = "e2m1", "e2m1", "mx", "mx", "f32"
+        elif name == "mxfp8_ffn_up":
+            self.fa, self.fb, self.ga, self.gb, self.out = "e4m3", "e4m3", "mx", "mx", "bf16"
         else:
             self.fa, self.fb, self.ga, self.gb, self.out = "e2m1", "e2m1", "mx", "mx", "bf16"
         self.A_host = A
@@ -140,6 +151,8 @@ class Workload:
         # weights are quantised once, outside the step (static parameters)
         if self.fp4:
             qb, sb = bsg.bsg_quantize_mxfp4(Bt, "tcgen05")
+        elif self.mx8:
+            qb, sb = bsg.bsg_quantize_mx(Bt, self.fb, "tcgen05")
         else:
             qb, sb = bsg.bsg_quantize_fp8(Bt, self.fb, self.gb)
         del Bt
@@ -155,6 +168,8 @@ class Workload:
                   "qb": qb if r == 0 else qb.clone(), "sb": sb if r == 0 else sb.clone()}
             if self.fp4:
                 st["qa"], st["sa"] = bsg.bsg_quantize_mxfp4(st["A"], "tcgen05")
+            elif self.mx8:
+                st["qa"], st["sa"] = bsg.bsg_quantize_mx(st["A"], self.fa, "tcgen05")
             else:
                 st["qa"], st["sa"] = bsg.bsg_quantize_fp8(st["A"], self.fa, self.ga)
             st["D"] = torch.empty((M, N), dtype=torch.bfloat16 if self.out == "bf16" else torch.float32,
@@ -169,6 +184,8 @@ class Workload:
         b, st = self.bsg, self.sets[r]
         if self.fp4:
             b.bsg_quantize_mxfp4(st["A"], "tcgen05", q=st["qa"], sf=st["sa"])
+        elif self.mx8:
+            b.bsg_quantize_mx(st["A"], self.fa, "tcgen05", q=st["qa"], sf=st["sa"])
         else:
             b.bsg_quantize_fp8(st["A"], self.fa, self.ga, q=st["qa"], scales=st["sa"])
 
@@ -193,6 +210,9 @@ class Workload:
         if self.fp4:
             a = M * K / 2 + M * K / 32
             b = N * K / 2 + N * K / 32
+        elif self.mx8:
+            a = M * K + M * K / 32
+            b = N * K + N * K / 32
         else:
             a = M * K + (M * -(-K // 128) * 4 if self.ga == "row" else 4 * -(-M // 128) * -(-K // 128))
             b = N * K + 4 * -(-N // 128) * -(-K // 128)
@@ -275,7 +295,7 @@ def cpu_baseline(name, m_override, target_s=15.0):
     """The CPU oracle as it stands, on a bounded sample of the workload."""
     import oracle.gemm as og
     import oracle.quantize as oq
-    idx, M, N, K = synth.WORKLOADS[name]
+    idx, M, N, K = synth.WORKLOADS[SHAPE_OF.get(name, name)]
     if m_override is not None:
         M = m_override
     cores = os.cpu_count()
@@ -293,6 +313,20 @@ def cpu_baseline(name, m_override, target_s=15.0):
         return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
                 "sample": f"decode M={M}, {nrows} of {N} weight rows, K={K}: oracle quantise + GEMM, "
                           f"{dt:.1f} s"}
+    if name == "mxfp8_ffn_up":
+        # the MX oracle picks every block's scale in a Python loop: a slice of
+        # B's rows keeps the sample bounded
+        rows, ncols = 128, 2048
+        A, B = synth.make("ffn_up", m=rows, n=ncols)
+        t0 = time.perf_counter()
+        qa, sfa = oq.quantize_mxfp8(A, "e4m3")
+        qb, sfb = oq.quantize_mxfp8(B, "e4m3")
+        og.gemm_mxfp8(qa, "e4m3", sfa, qb, "e4m3", sfb)
+        dt = time.perf_counter() - t0
+        return {"value": 2.0 * rows * ncols * K / dt / 1e12, "unit": "TFLOP/s", "cores": cores,
+                "kind": "oracle",
+                "sample": f"{name}: {rows} of {M} rows of A with {ncols} of {N} rows of B (K={K}); "
+                          f"oracle MXFP8 quantise (both operands) + FP64 GEMM, {dt:.1f} s"}
     fa, fb, ga, gb = {"ffn_up": ("e4m3", "e4m3", "row", "tile"),
                       "dgrad": ("e5m2", "e4m3", "tile", "tile"),
                       "fp8_256": ("e4m3", "e4m3", "tile", "tile"),
@@ -339,7 +373,7 @@ def run_reference(args, world, rank):
     for _ in range(max(1, min(args.steps, 3))):
         vals.append(cpu_baseline(args.workload, args.m)["value"])
     v = statistics.median(vals)
-    idx, M, N, K = synth.WORKLOADS[args.workload]
+    idx, M, N, K = synth.WORKLOADS[SHAPE_OF.get(args.workload, args.workload)]
     metric = ("GB/s of algorithmic bytes (decode M<=16, % of HBM)" if args.workload == "decode"
               else "GEMM TFLOP/s (% of GB300 dense FP8/FP4 peak)")
     line = {"impl": "reference", "metric": metric, "value": v, "unit": cb["unit"],
@@ -508,9 +542,11 @@ def main():
         dt = "fp4" if w.fp4 else "fp8"
         achieved = w.flops() / g_s / 1e12
         peak = pk["bf16_tflops"] * RATIO[dt]
+        src_kind = "mx8" if w.mx8 else dt
+        kernel = "gemm_mxfp4_kernel" if w.fp4 else ("gemm_mx_kernel" if w.mx8 else "gemm_fp8_kernel")
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": measured_traffic(w.name, dt),
-                "kernel": "gemm_mxfp4_kernel" if w.fp4 else "gemm_fp8_kernel",
+                "frac": achieved / peak, "traffic": measured_traffic(w.name, src_kind),
+                "kernel": kernel,
                 "peak_source": f"{pk_kind} cuBLAS BF16 burst x {RATIO[dt]:g} (nominal dense "
                                f"{dt.upper()}:BF16 ratio)"}
     metric, unit = w.metric()

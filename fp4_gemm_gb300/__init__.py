@@ -32,7 +32,7 @@ LAYOUT = {"rowmajor": 0, "tcgen05": 1}
 
 EXPORTS = ("bsg_quantize_fp8", "bsg_quantize_mxfp4", "bsg_gemm", "bsg_gemm_workspace_size",
            "bsg_scale_bytes", "bsg_sf_to_tcgen05", "bsg_status_string", "bsg_device_error",
-           "bsg_num_sms", "bsg_gemm_decode_noalloc", "bsg_mma_peak")
+           "bsg_num_sms", "bsg_gemm_decode_noalloc", "bsg_mma_peak", "bsg_quantize_mx")
 
 
 class BsgError(RuntimeError):
@@ -75,7 +75,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsg_num_sms.restype = i32
     lib.bsg_gemm_decode_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, vp, i32, vp]
     lib.bsg_gemm_decode_noalloc.restype = i32
-    lib.bsg_mma_peak.argtypes = [i32, i32, i64, c.POINTER(i64), vp]
+    lib.bsg_quantize_mx.argtypes = [vp, i32, i64, i64, i64, i32, f32, vp, vp, i32, vp]
+    lib.bsg_quantize_mx.restype = i32
+    lib.bsg_mma_peak.argtypes = [i32, i32, i32, i64, c.POINTER(i64), vp]
     lib.bsg_mma_peak.restype = i32
     _lib = lib
     return lib
@@ -114,13 +116,15 @@ def bsg_num_sms() -> int:
     return int(load_library().bsg_num_sms())
 
 
-def bsg_mma_peak(fmt: str = "e4m3", pair: bool = False, iters: int = 1 << 16, stream=None) -> int:
+def bsg_mma_peak(fmt: str = "e4m3", pair: bool = False, iters: int = 1 << 16,
+                 block_scaled: bool = False, stream=None) -> int:
     """Launch the tensor-core throughput microbenchmark on `stream` (or the
     current stream) and return the FLOPs the launch performs; the caller
-    times it with CUDA events.  fmt "e4m3" (kind::f8f6f4) or "e2m1"
-    (block-scaled kind::mxf4)."""
+    times it with CUDA events.  fmt "e4m3" (kind::f8f6f4, or with
+    block_scaled kind::mxf8f6f4) or "e2m1" (block-scaled kind::mxf4)."""
     flops = ctypes.c_int64(0)
-    _check(load_library().bsg_mma_peak(FORMAT[fmt], 1 if pair else 0, int(iters),
+    bs = 1 if (block_scaled or fmt == "e2m1") else 0
+    _check(load_library().bsg_mma_peak(FORMAT[fmt], bs, 1 if pair else 0, int(iters),
                                        ctypes.byref(flops), _stream(stream)), "bsg_mma_peak")
     return int(flops.value)
 
@@ -180,6 +184,35 @@ def bsg_quantize_mxfp4(x: torch.Tensor, layout: str = "tcgen05", q: torch.Tensor
     _need_cuda(x, q, sf)
     _check(lib.bsg_quantize_mxfp4(_ptr(x), src, rows, cols, x.stride(0), _ptr(q), _ptr(sf),
                                   LAYOUT[layout], _stream(stream)), "bsg_quantize_mxfp4")
+    return q, sf
+
+
+def bsg_quantize_mx(x: torch.Tensor, fmt: str = "e4m3", layout: str = "tcgen05",
+                    fmt_max: float = 0.0, q: torch.Tensor | None = None,
+                    sf: torch.Tensor | None = None, stream=None):
+    """MX quantisation, x: (rows, K) FP32 or BF16 CUDA tensor, K % 32 == 0.
+    fmt "e4m3" / "e5m2" (MXFP8: codes uint8 (rows, K)) or "e2m1" (MXFP4:
+    packed uint8 (rows, K/2)).  Returns (codes, E8M0 scales); "rowmajor"
+    scales are (rows, K/32), "tcgen05" scales a flat buffer in the MMA's
+    atom order."""
+    lib = load_library()
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D tensor with unit column stride")
+    rows, cols = x.shape
+    src = {torch.float32: 0, torch.bfloat16: 1}[x.dtype]
+    if q is None:
+        q = torch.empty((rows, cols // 2 if fmt == "e2m1" else cols), dtype=torch.uint8,
+                        device=x.device)
+    if sf is None:
+        if layout == "rowmajor":
+            sf = torch.empty((rows, cols // 32), dtype=torch.uint8, device=x.device)
+        else:
+            n = lib.bsg_scale_bytes(rows, cols, GRAN["mx"], LAYOUT["tcgen05"])
+            sf = torch.empty((max(int(n), 1),), dtype=torch.uint8, device=x.device)
+    _need_cuda(x, q, sf)
+    _check(lib.bsg_quantize_mx(_ptr(x), src, rows, cols, x.stride(0), FORMAT[fmt], float(fmt_max),
+                               _ptr(q), _ptr(sf), LAYOUT[layout], _stream(stream)),
+           "bsg_quantize_mx")
     return q, sf
 
 

@@ -169,18 +169,30 @@ bsg_status bsg_quantize_fp8(const void* x, bsg_dtype src, int64_t rows, int64_t 
       bsg::launch_quantize_fp8_row(x, src == BSG_BF16, rows, cols, ld, f, fm, q, scales, s));
 }
 
-bsg_status bsg_quantize_mxfp4(const void* x, bsg_dtype src, int64_t rows, int64_t cols,
-                              int64_t ld, uint8_t* q_packed, uint8_t* sf, bsg_sf_layout layout,
-                              void* stream) {
-  if (x == nullptr || q_packed == nullptr || sf == nullptr) return BSG_ERR_INVALID_ARG;
+bsg_status bsg_quantize_mx(const void* x, bsg_dtype src, int64_t rows, int64_t cols, int64_t ld,
+                           bsg_format fmt, float fmt_max, uint8_t* q, uint8_t* sf,
+                           bsg_sf_layout layout, void* stream) {
+  if (x == nullptr || q == nullptr || sf == nullptr) return BSG_ERR_INVALID_ARG;
   if (rows <= 0 || cols <= 0 || ld < cols || rows > kMaxDim || cols > kMaxDim || cols % 32)
     return BSG_ERR_INVALID_ARG;
   if (src != BSG_F32 && src != BSG_BF16) return BSG_ERR_INVALID_ARG;
   if (layout != BSG_SF_ROWMAJOR && layout != BSG_SF_TCGEN05) return BSG_ERR_INVALID_ARG;
-  if (!aligned(x, src == BSG_F32 ? 4 : 2) || !aligned(q_packed, 4)) return BSG_ERR_ALIGNMENT;
-  return from_cuda(bsg::launch_quantize_mxfp4(x, src == BSG_BF16, rows, cols, ld, q_packed, sf,
-                                              layout == BSG_SF_TCGEN05,
-                                              static_cast<cudaStream_t>(stream)));
+  if (!(fmt_max >= 0.0f) || !std::isfinite(fmt_max)) return BSG_ERR_INVALID_ARG;
+  if (fmt != BSG_E4M3 && fmt != BSG_E5M2 && fmt != BSG_E2M1) return BSG_ERR_INVALID_ARG;
+  if (!aligned(x, src == BSG_F32 ? 4 : 2) || !aligned(q, fmt == BSG_E2M1 ? 4 : 8))
+    return BSG_ERR_ALIGNMENT;
+  const float fm = fmt_max != 0.0f ? fmt_max
+                                   : (fmt == BSG_E2M1 ? 6.0f : (fmt == BSG_E4M3 ? 448.0f : 57344.0f));
+  const int f = fmt == BSG_E4M3 ? 0 : (fmt == BSG_E5M2 ? 1 : 2);
+  return from_cuda(bsg::launch_quantize_mx(x, src == BSG_BF16, rows, cols, ld, f, fm, q, sf,
+                                           layout == BSG_SF_TCGEN05,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+bsg_status bsg_quantize_mxfp4(const void* x, bsg_dtype src, int64_t rows, int64_t cols,
+                              int64_t ld, uint8_t* q_packed, uint8_t* sf, bsg_sf_layout layout,
+                              void* stream) {
+  return bsg_quantize_mx(x, src, rows, cols, ld, BSG_E2M1, 0.0f, q_packed, sf, layout, stream);
 }
 
 bsg_status bsg_sf_to_tcgen05(const uint8_t* sf_rowmajor, int64_t rows, int64_t kblocks,
@@ -218,7 +230,13 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
   const bool fp8 = is_fp8(fa) && is_fp8(fb);
   const bool fp4 = fa == BSG_E2M1 && fb == BSG_E2M1;
   if (!fp8 && !fp4) return BSG_ERR_UNSUPPORTED;
-  if (fp8) {
+  // FP8 operands take FP32 per-tile scales (promoted FP8 GEMM) or, both of
+  // them, E8M0 scales per 32 along K (MXFP8)
+  const bool mx8 = fp8 && ga == BSG_SCALE_BLOCK1x32_E8M0 && gb == BSG_SCALE_BLOCK1x32_E8M0;
+  if (mx8) {
+    if (K % 32) return BSG_ERR_INVALID_ARG;
+    if (!aligned(sA, 16) || !aligned(sB, 16)) return BSG_ERR_ALIGNMENT;
+  } else if (fp8) {
     if (ga != BSG_SCALE_TILE128x128 && ga != BSG_SCALE_ROW1x128) return BSG_ERR_UNSUPPORTED;
     if (gb != BSG_SCALE_TILE128x128 && gb != BSG_SCALE_ROW1x128) return BSG_ERR_UNSUPPORTED;
     if (K % 16) return BSG_ERR_INVALID_ARG;
@@ -232,6 +250,24 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
   const int sms = num_sms_current();
   if (sms <= 0) return BSG_ERR_CUDA;
 
+  if (mx8) {
+    bsg::MxGemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.afmt = fa == BSG_E4M3 ? 0 : 1;
+    a.bfmt = fb == BSG_E4M3 ? 0 : 1;
+    a.sfA = static_cast<const uint8_t*>(sA);
+    a.sfB = static_cast<const uint8_t*>(sB);
+    a.C = C;
+    a.D = D;
+    a.out_bf16 = out == BSG_BF16;
+    if (!make_kmajor_map(&a.tmA, A, K, M, K, 128) ||
+        !make_kmajor_map(&a.tmB, B, K, N, K, static_cast<uint32_t>(bsg::gemm_mx_b_box_rows())))
+      return BSG_ERR_CUDA;
+    return from_cuda(bsg::launch_gemm_mx(a, sms, s));
+  }
   if (fp8) {
     Fp8GemmArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -288,24 +324,33 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
 bsg_status bsg_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return BSG_ERR_CUDA;
-  uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
+  uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0, w4 = 0;
   if (bsg::quantize_error_read_and_clear(s, &w0) != cudaSuccess ||
       bsg::gemm_fp8_error_read_and_clear(s, &w1) != cudaSuccess ||
       bsg::gemm_mxfp4_error_read_and_clear(s, &w2) != cudaSuccess ||
-      bsg::mma_peak_error_read_and_clear(s, &w3) != cudaSuccess)
+      bsg::mma_peak_error_read_and_clear(s, &w3) != cudaSuccess ||
+      bsg::gemm_mx_error_read_and_clear(s, &w4) != cudaSuccess)
     return BSG_ERR_CUDA;
-  const uint32_t w = w0 | w1 | w2 | w3;
+  const uint32_t w = w0 | w1 | w2 | w3 | w4;
   if (w & 1u) return BSG_ERR_TIMEOUT;
   if (w & 2u) return BSG_ERR_WORKSPACE;
   return BSG_OK;
 }
 
-bsg_status bsg_mma_peak(bsg_format fmt, int pair, int64_t iters, int64_t* flops, void* stream) {
+bsg_status bsg_mma_peak(bsg_format fmt, int block_scaled, int pair, int64_t iters, int64_t* flops,
+                        void* stream) {
   if (flops == nullptr || iters <= 0 || iters > kMaxPeakIters) return BSG_ERR_INVALID_ARG;
-  if (fmt != BSG_E4M3 && fmt != BSG_E2M1) return BSG_ERR_UNSUPPORTED;
+  int kind;
+  if (fmt == BSG_E4M3)
+    kind = block_scaled ? 1 : 0;
+  else if (fmt == BSG_E2M1 && block_scaled)
+    kind = 2;
+  else
+    return BSG_ERR_UNSUPPORTED;
+  if (kind == 1 && pair) return BSG_ERR_UNSUPPORTED;
   const int sms = num_sms_current();
   if (sms <= 0 || (pair && sms < 2)) return BSG_ERR_CUDA;
-  return from_cuda(bsg::launch_mma_peak(fmt == BSG_E2M1, pair != 0, iters, sms,
+  return from_cuda(bsg::launch_mma_peak(kind, pair != 0, iters, sms,
                                         static_cast<cudaStream_t>(stream), flops));
 }
 

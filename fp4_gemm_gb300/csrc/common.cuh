@@ -389,6 +389,20 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// Block-scaled FP8 MMA: E4M3 / E5M2 operands, one UE8M0 scale per 32 K per
+// row (scale_vec::1X: K = 32 per instruction, so one scale byte per row,
+// selected by the scale-factor ids of the instruction descriptor).
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Copy a 32-row x 16-byte matrix from smem into tensor memory, replicated to
 // the four 32-lane quarters (the scale-factor copy of block-scaled MMA).
 __device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
@@ -534,6 +548,19 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N, uint32
                                                   uint32_t sfb_id) {
   return (sfb_id << 4)              // B scale-factor id
          | (1u << 7) | (1u << 10)   // A, B = E2M1
+         | ((N >> 3) << 17)         // N / 8
+         | (1u << 23)               // scale type UE8M0
+         | ((M >> 4) << 24)         // M / 16
+         | (sfa_id << 29);          // A scale-factor id
+}
+
+// Instruction descriptor for kind::mxf8f6f4 block-scaled MMA: FP8 operands
+// (0 = E4M3, 1 = E5M2), UE8M0 scales, K-major operands; sf ids select the
+// byte of the 32-bit scale column each operand's scales start at.
+__host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t afmt, uint32_t bfmt, uint32_t M,
+                                                  uint32_t N, uint32_t sfa_id, uint32_t sfb_id) {
+  return (sfb_id << 4)              // B scale-factor id
+         | (afmt << 7) | (bfmt << 10)  // A, B formats
          | ((N >> 3) << 17)         // N / 8
          | (1u << 23)               // scale type UE8M0
          | ((M >> 4) << 24)         // M / 16

@@ -15,6 +15,7 @@ cudaError_t quantize_error_read_and_clear(cudaStream_t s, uint32_t* out);
 cudaError_t gemm_fp8_error_read_and_clear(cudaStream_t s, uint32_t* out);
 cudaError_t gemm_mxfp4_error_read_and_clear(cudaStream_t s, uint32_t* out);
 cudaError_t mma_peak_error_read_and_clear(cudaStream_t s, uint32_t* out);
+cudaError_t gemm_mx_error_read_and_clear(cudaStream_t s, uint32_t* out);
 
 // ------------------------------------------------------------- quantisers
 // src_bf16: source is BF16 (else FP32).  fmt: 0 E4M3, 1 E5M2.
@@ -24,11 +25,13 @@ cudaError_t launch_quantize_fp8_tile(const void* x, bool src_bf16, int64_t rows,
 cudaError_t launch_quantize_fp8_row(const void* x, bool src_bf16, int64_t rows, int64_t cols,
                                     int64_t ld, int fmt, float fmt_max, uint8_t* q, float* scales,
                                     cudaStream_t s);
+// MX quantiser.  fmt: 0 E4M3, 1 E5M2 (MXFP8, one code per byte), 2 E2M1
+// (MXFP4, two codes per byte); fmt_max: the value a block maximum maps to.
 // tc_layout: write scales in the tcgen05 atom layout (with padding) instead
 // of row-major.
-cudaError_t launch_quantize_mxfp4(const void* x, bool src_bf16, int64_t rows, int64_t cols,
-                                  int64_t ld, uint8_t* q, uint8_t* sf, bool tc_layout,
-                                  cudaStream_t s);
+cudaError_t launch_quantize_mx(const void* x, bool src_bf16, int64_t rows, int64_t cols,
+                               int64_t ld, int fmt, float fmt_max, uint8_t* q, uint8_t* sf,
+                               bool tc_layout, cudaStream_t s);
 cudaError_t launch_sf_to_tcgen05(const uint8_t* sf, int64_t rows, int64_t kblocks, uint8_t* out,
                                  cudaStream_t s);
 
@@ -69,6 +72,20 @@ bool gemm_fp8_use_pair(int M, int N, int num_sms);
 int gemm_fp8_b_box_rows(bool pair);
 cudaError_t launch_gemm_fp8(const Fp8GemmArgs& a, int num_sms, cudaStream_t s);
 
+// MXFP8 GEMM (FP8 operands, E8M0 scales per 32 along K in the tcgen05 layout).
+struct MxGemmArgs {
+  int M, N, K;
+  int afmt, bfmt;            // 0 E4M3, 1 E5M2
+  const uint8_t* sfA;
+  const uint8_t* sfB;
+  const float* C;
+  void* D;
+  bool out_bf16;
+  CUtensorMap tmA, tmB;      // A: box 128 B x 128 rows; B: box 128 B x gemm_mx_b_box_rows()
+};
+int gemm_mx_b_box_rows();
+cudaError_t launch_gemm_mx(const MxGemmArgs& a, int num_sms, cudaStream_t s);
+
 struct Mxfp4GemmArgs {
   int M, N, K;
   const uint8_t* sfA;        // tcgen05 layout
@@ -90,8 +107,9 @@ cudaError_t launch_gemm_mxfp4_decode(const Mxfp4GemmArgs& a, int num_sms, cudaSt
 
 // ------------------------------------------------- tensor-core microbenchmark
 // Back-to-back tcgen05.mma from shared memory on every SM; *flops receives
-// the floating-point operations the launch performs.
-cudaError_t launch_mma_peak(bool fp4, bool pair, int64_t iters, int num_sms, cudaStream_t s,
+// the floating-point operations the launch performs.  kind: 0 dense FP8,
+// 1 block-scaled FP8 (single CTA only), 2 block-scaled FP4.
+cudaError_t launch_mma_peak(int kind, bool pair, int64_t iters, int num_sms, cudaStream_t s,
                             int64_t* flops);
 
 }  // namespace bsg

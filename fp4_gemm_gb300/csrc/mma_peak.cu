@@ -1,5 +1,6 @@
-// Tensor-core throughput microbenchmark: the dense FP8 and block-scaled FP4
-// rates of tcgen05.mma on this GPU, at whatever clock it runs at.
+// Tensor-core throughput microbenchmark: the dense FP8, block-scaled FP8 and
+// block-scaled FP4 rates of tcgen05.mma on this GPU, at whatever clock it
+// runs at.
 //
 // The GEMM kernels of this library are reported against a peak.  The FP8 and
 // FP4 peaks of GB300 are not given by any measured copy or library GEMM on
@@ -8,6 +9,8 @@
 // operands already sit in shared memory - no global traffic, no epilogue.
 //   FP8:  tcgen05.mma kind::f8f6f4, E4M3 x E4M3, M128 N256 K32 per
 //         instruction (M256 for a CTA pair, cta_group::2).
+//   MXFP8: tcgen05.mma kind::mxf8f6f4.block_scale.scale_vec::1X, E4M3 x E4M3
+//         with UE8M0 scales, M128 N256 K32 per instruction.
 //   FP4:  tcgen05.mma kind::mxf4.block_scale.scale_vec::2X, E2M1 x E2M1 with
 //         UE8M0 scales, M128 N256 K64 per instruction (M256 for a pair).
 // The operand tiles are zero-filled; scales are whatever tensor memory holds.
@@ -23,13 +26,14 @@ __device__ uint32_t g_peak_error = 0;
 constexpr int kPeakThreads = 128;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 256;           // N = 256 FP32 accumulator columns
-constexpr int kSfaCol = 256;            // scale columns (FP4 only)
+constexpr int kSfaCol = 256;            // scale columns (block-scaled kinds)
 constexpr int kSfbCol = 288;
 // Dynamic shared memory requested per CTA: large enough that only one CTA
 // fits on an SM, so each SM's tensor memory has a single owner.
 constexpr size_t kPeakSmem = 150 * 1024;
 
-template <bool kPair, bool kFp4>
+// kKind: 0 dense FP8, 1 block-scaled FP8 (MXFP8), 2 block-scaled FP4 (MXFP4)
+template <bool kPair, int kKind>
 __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int64_t iters) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -69,16 +73,20 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int64_t iters
     const uint64_t ad = sdesc_kmajor_sw128(smem_u32(a));
     const uint64_t bd = sdesc_kmajor_sw128(smem_u32(b));
     constexpr uint32_t M = kPair ? 256 : 128;
-    const uint32_t id = kFp4 ? idesc_mxf4(M, kAccCols, 0, 0) : idesc_f8f6f4(0, 0, M, kAccCols);
+    const uint32_t id = kKind == 2   ? idesc_mxf4(M, kAccCols, 0, 0)
+                        : kKind == 1 ? idesc_mxf8(0, 0, M, kAccCols, 0, 0)
+                                     : idesc_f8f6f4(0, 0, M, kAccCols);
     for (int64_t i = 0; i < iters; ++i) {
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-        if (kFp4) {
+        if (kKind == 2) {
           if (kPair)
             mma_mxf4_pair(tmem, ad + 2 * kk, bd + 2 * kk, id, tmem + kSfaCol, tmem + kSfbCol, acc);
           else
             mma_mxf4(tmem, ad + 2 * kk, bd + 2 * kk, id, tmem + kSfaCol, tmem + kSfbCol, acc);
+        } else if (kKind == 1) {
+          mma_mxf8(tmem, ad + 2 * kk, bd + 2 * kk, id, tmem + kSfaCol, tmem + kSfbCol, acc);
         } else {
           if (kPair)
             mma_f8f6f4_pair(tmem, ad + 2 * kk, bd + 2 * kk, id, acc);
@@ -106,9 +114,10 @@ __global__ void __launch_bounds__(kPeakThreads, 1) mma_peak_kernel(int64_t iters
   if (kPair) cluster_sync();
 }
 
-template <bool kPair, bool kFp4>
+template <bool kPair, int kKind>
 cudaError_t launch_peak(int64_t iters, int num_sms, cudaStream_t s, int64_t* flops) {
-  auto kern = mma_peak_kernel<kPair, kFp4>;
+  constexpr bool kFp4 = kKind == 2;
+  auto kern = mma_peak_kernel<kPair, kKind>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kPeakSmem));
   if (e != cudaSuccess) return e;
@@ -149,12 +158,15 @@ cudaError_t mma_peak_error_read_and_clear(cudaStream_t s, uint32_t* out) {
   return cudaStreamSynchronize(s);
 }
 
-cudaError_t launch_mma_peak(bool fp4, bool pair, int64_t iters, int num_sms, cudaStream_t s,
+cudaError_t launch_mma_peak(int kind, bool pair, int64_t iters, int num_sms, cudaStream_t s,
                             int64_t* flops) {
-  if (fp4) return pair ? launch_peak<true, true>(iters, num_sms, s, flops)
-                       : launch_peak<false, true>(iters, num_sms, s, flops);
-  return pair ? launch_peak<true, false>(iters, num_sms, s, flops)
-              : launch_peak<false, false>(iters, num_sms, s, flops);
+  switch (kind) {
+    case 0: return pair ? launch_peak<true, 0>(iters, num_sms, s, flops)
+                        : launch_peak<false, 0>(iters, num_sms, s, flops);
+    case 1: return launch_peak<false, 1>(iters, num_sms, s, flops);
+    default: return pair ? launch_peak<true, 2>(iters, num_sms, s, flops)
+                         : launch_peak<false, 2>(iters, num_sms, s, flops);
+  }
 }
 
 }  // namespace bsg

@@ -12,7 +12,8 @@
 // v (linear distance, ties to the larger), read off v's exponent field and its
 // first mantissa bit; elements are multiplied by the exact inverse power of
 // two and converted with cvt.rn.satfinite.e2m1x2; two codes per byte, the
-// first element in the low nibble.
+// first element in the low nibble.  MXFP8 applies the same rule with the FP8
+// format's largest value in place of 6 and E4M3 / E5M2 elements.
 //
 // All kernels are single-pass and HBM-bound: each element is read once and
 // its code written once.
@@ -269,12 +270,14 @@ __device__ __forceinline__ int64_t sf_tc_offset(int64_t row, int64_t b, int64_t 
          (b & 3);
 }
 
-// One warp per (row, 256-column chunk); lane l owns 8 elements, 4 lanes per
-// 32-element block.  In the tcgen05 layout the grid also covers the padding
-// rows / K-blocks of the last atoms and writes 127 there.
-template <bool kBF16, bool kTC>
-__global__ void __launch_bounds__(256) quantize_mxfp4_kernel(
-    const void* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, bool vec_in,
+// MX quantiser: one warp per (row, 256-column chunk); lane l owns 8
+// elements, 4 lanes per 32-element block.  kFmt 2: E2M1 codes packed two per
+// byte (MXFP4); kFmt 0 / 1: E4M3 / E5M2 codes, one per byte (MXFP8).  In the
+// tcgen05 layout the grid also covers the padding rows / K-blocks of the last
+// atoms and writes 127 there.
+template <bool kBF16, bool kTC, int kFmt>
+__global__ void __launch_bounds__(256) quantize_mx_kernel(
+    const void* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, float fmt_max, bool vec_in,
     uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
   grid_dep_launch();
   grid_dep_wait();
@@ -302,15 +305,22 @@ __global__ void __launch_bounds__(256) quantize_mxfp4_kernel(
   for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-  const uint32_t code = e8m0_nearest(__fdiv_rn(amax, 6.0f));
+  const uint32_t code = e8m0_nearest(__fdiv_rn(amax, fmt_max));
   if (data) {
     // 2^-(code-127) as an FP32 normal: code in [0,254] -> exponent field 254-code
     const float inv = __uint_as_float(static_cast<uint32_t>(254 - static_cast<int>(code)) << 23);
-    uint32_t packed = 0;
+    if (kFmt == 2) {
+      uint32_t packed = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      packed |= cvt2_e2m1(v[2 * j] * inv, v[2 * j + 1] * inv) << (8 * j);
-    *reinterpret_cast<uint32_t*>(q + row * (cols / 2) + col / 2) = packed;
+      for (int j = 0; j < 4; ++j)
+        packed |= cvt2_e2m1(v[2 * j] * inv, v[2 * j + 1] * inv) << (8 * j);
+      *reinterpret_cast<uint32_t*>(q + row * (cols / 2) + col / 2) = packed;
+    } else {
+      uint2 c;
+      c.x = cvt4_fp8(kFmt, v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
+      c.y = cvt4_fp8(kFmt, v[4] * inv, v[5] * inv, v[6] * inv, v[7] * inv);
+      *reinterpret_cast<uint2*>(q + row * cols + col) = c;
+    }
   }
   if ((lane & 3) == 0 && b < kb_pad) {
     const uint8_t c = data ? static_cast<uint8_t>(code) : static_cast<uint8_t>(127);
@@ -374,18 +384,27 @@ cudaError_t launch_quantize_fp8_row(const void* x, bool src_bf16, int64_t rows, 
                     vec_in, vec_out, q, scales);
 }
 
-cudaError_t launch_quantize_mxfp4(const void* x, bool src_bf16, int64_t rows, int64_t cols,
-                                  int64_t ld, uint8_t* q, uint8_t* sf, bool tc_layout,
-                                  cudaStream_t s) {
+cudaError_t launch_quantize_mx(const void* x, bool src_bf16, int64_t rows, int64_t cols,
+                               int64_t ld, int fmt, float fmt_max, uint8_t* q, uint8_t* sf,
+                               bool tc_layout, cudaStream_t s) {
   const bool vec_in = src_bf16 ? (aligned(x, 8) && ld % 4 == 0) : (aligned(x, 16) && ld % 4 == 0);
   const int64_t kb = cols / 32;
   const int64_t kb_pad = tc_layout ? ((kb + 3) / 4) * 4 : kb;
   const int64_t rows_pad = tc_layout ? ((rows + 127) / 128) * 128 : rows;
   const int64_t warps = rows_pad * ((kb_pad + 7) / 8);
   const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
-  auto kern = src_bf16 ? (tc_layout ? quantize_mxfp4_kernel<true, true> : quantize_mxfp4_kernel<true, false>)
-                       : (tc_layout ? quantize_mxfp4_kernel<false, true> : quantize_mxfp4_kernel<false, false>);
-  return launch_pdl(kern, dim3(blocks), dim3(256), 0, s, x, rows, cols, ld, vec_in, q, sf);
+  using K = void (*)(const void*, int64_t, int64_t, int64_t, float, bool, uint8_t*, uint8_t*);
+  // [fmt][bf16][tc]
+  static const K table[3][2][2] = {
+      {{quantize_mx_kernel<false, false, 0>, quantize_mx_kernel<false, true, 0>},
+       {quantize_mx_kernel<true, false, 0>, quantize_mx_kernel<true, true, 0>}},
+      {{quantize_mx_kernel<false, false, 1>, quantize_mx_kernel<false, true, 1>},
+       {quantize_mx_kernel<true, false, 1>, quantize_mx_kernel<true, true, 1>}},
+      {{quantize_mx_kernel<false, false, 2>, quantize_mx_kernel<false, true, 2>},
+       {quantize_mx_kernel<true, false, 2>, quantize_mx_kernel<true, true, 2>}}};
+  if (fmt < 0 || fmt > 2) return cudaErrorInvalidValue;
+  const K kern = table[fmt][src_bf16 ? 1 : 0][tc_layout ? 1 : 0];
+  return launch_pdl(kern, dim3(blocks), dim3(256), 0, s, x, rows, cols, ld, fmt_max, vec_in, q, sf);
 }
 
 cudaError_t launch_sf_to_tcgen05(const uint8_t* sf, int64_t rows, int64_t kblocks, uint8_t* out,

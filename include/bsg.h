@@ -134,6 +134,29 @@ bsg_status bsg_quantize_mxfp4(const void* x, bsg_dtype src, int64_t rows, int64_
                               int64_t ld, uint8_t* q_packed, uint8_t* sf,
                               bsg_sf_layout layout, void* stream);
 
+/* bsg_quantize_mx - MX quantisation with E2M1 (MXFP4) or FP8 (MXFP8) elements.
+ *
+ * "Rubin FP4 GEMM deep dive", section 2.2 (32 consecutive elements along K
+ * share one E8M0 scale) and section 4.2 steps 1-3, with the element format's
+ * largest value in place of E2M1's 6 for FP8 elements: per block,
+ * v = max|x| / fmt_max (FP32), the E8M0 scale is the power of two nearest to v
+ * (as bsg_quantize_mxfp4), and each element times the inverse power of two
+ * (exact) is rounded to the element format (nearest, ties to even,
+ * saturating).  Taking the E2M1 rule unchanged for FP8 elements is a reading.
+ *
+ * fmt      BSG_E2M1 (codes packed two per byte, first element in the low
+ *          nibble: rows x cols/2 bytes), BSG_E4M3 or BSG_E5M2 (one code per
+ *          byte: rows x cols bytes).
+ * fmt_max  0 selects the format's own maximum (6, 448, 57344); otherwise any
+ *          positive finite value.
+ * Other arguments as bsg_quantize_mxfp4.  q must be 8-byte aligned for FP8.
+ * Errors: BSG_ERR_INVALID_ARG (null, sizes, cols % 32, bad fmt or fmt_max),
+ *         BSG_ERR_ALIGNMENT, BSG_ERR_CUDA.
+ */
+bsg_status bsg_quantize_mx(const void* x, bsg_dtype src, int64_t rows, int64_t cols, int64_t ld,
+                           bsg_format fmt, float fmt_max, uint8_t* q, uint8_t* sf,
+                           bsg_sf_layout layout, void* stream);
+
 /* bsg_gemm - block-scaled GEMM D = sum_k (s_A a_k)(s_B b_k) + C.
  *
  * "FP8 GEMM on CDNA4", sections 2.2 (FP32 accumulation), 3.3 and 4.4 (the
@@ -150,7 +173,10 @@ bsg_status bsg_quantize_mxfp4(const void* x, bsg_dtype src, int64_t rows, int64_
  * B   device, K x N column-major = N x K row-major, same encoding rules.
  * fa, fb  operand formats: both FP8 (E4M3 / E5M2, any mix) or both E2M1.
  * sA, ga  A's scales: FP8 -> BSG_SCALE_TILE128x128 ([ceil(M/128)][ceil(K/128)])
- *         or BSG_SCALE_ROW1x128 ([ceil(K/128)][M]); E2M1 ->
+ *         or BSG_SCALE_ROW1x128 ([ceil(K/128)][M]) (FP32 scales, promoted per
+ *         128-wide K tile), or - for both operands together - MXFP8:
+ *         BSG_SCALE_BLOCK1x32_E8M0 in the BSG_SF_TCGEN05 layout (applied by
+ *         the tensor core, as bsg_quantize_mx writes them); E2M1 ->
  *         BSG_SCALE_BLOCK1x32_E8M0 in the BSG_SF_TCGEN05 layout.
  * sB, gb  B's scales, same rules with N in place of M.
  * C   device, optional (NULL) FP32 M x N row-major addend.
@@ -160,8 +186,8 @@ bsg_status bsg_quantize_mxfp4(const void* x, bsg_dtype src, int64_t rows, int64_
  *     NULL when that size is 0).  It must be zero-filled before its first use;
  *     the library leaves it zero-filled after every successful call.  Calls
  *     that share a workspace must not overlap in time.
- * Constraints: M, N, K > 0; K % 16 == 0 for FP8, K % 32 == 0 for E2M1; A, B,
- *     D, C 16-byte aligned.
+ * Constraints: M, N, K > 0; K % 16 == 0 for FP8 with FP32 scales, K % 32 == 0
+ *     for E8M0 scales; A, B 16-byte aligned (E8M0 scale arrays too).
  * Errors: BSG_ERR_INVALID_ARG, BSG_ERR_UNSUPPORTED, BSG_ERR_ALIGNMENT,
  *         BSG_ERR_WORKSPACE, BSG_ERR_CUDA.
  */
@@ -214,15 +240,18 @@ bsg_status bsg_gemm_decode_noalloc(int64_t M, int64_t N, int64_t K, const void* 
  * One launch keeps every SM's tensor core busy with `iters` x 4 back-to-back
  * MMAs whose operands sit in shared memory (zero-filled; no global memory
  * traffic, no epilogue; results discarded):
- *   fmt = BSG_E4M3: tcgen05.mma kind::f8f6f4, E4M3 x E4M3, M128 N256 K32;
- *   fmt = BSG_E2M1: tcgen05.mma kind::mxf4.block_scale, M128 N256 K64.
+ *   fmt = BSG_E4M3, block_scaled = 0: kind::f8f6f4, E4M3 x E4M3, M128 N256 K32;
+ *   fmt = BSG_E4M3, block_scaled = 1: kind::mxf8f6f4.block_scale (UE8M0
+ *         scales, scale_vec::1X), M128 N256 K32 (no CTA pairs);
+ *   fmt = BSG_E2M1, block_scaled = 1: kind::mxf4.block_scale, M128 N256 K64.
  * pair != 0 runs CTA pairs (cta_group::2, M256 per instruction).
  * *flops (host) receives the floating-point operations of the launch
  * (2*M*N*K per MMA); divide by the launch's duration, timed by the caller
  * with events on `stream`.
  * Errors: BSG_ERR_INVALID_ARG (null flops, iters <= 0 or > 2^20),
- *         BSG_ERR_UNSUPPORTED (other formats), BSG_ERR_CUDA. */
-bsg_status bsg_mma_peak(bsg_format fmt, int pair, int64_t iters, int64_t* flops, void* stream);
+ *         BSG_ERR_UNSUPPORTED (other combinations), BSG_ERR_CUDA. */
+bsg_status bsg_mma_peak(bsg_format fmt, int block_scaled, int pair, int64_t iters, int64_t* flops,
+                        void* stream);
 
 /* Human-readable name of a status. */
 const char* bsg_status_string(bsg_status status);
