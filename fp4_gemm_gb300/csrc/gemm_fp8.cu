@@ -253,38 +253,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------------- MMA
     setmaxnreg_dec<kRegsSmall>();
     if (lane == 0 && rank == 0) {
-      uint32_t it = 0;
-      bool ok = true;
-      for (int t = unit; t < tiles && ok; t += units) {
-        for (int kt = 0; kt < KT; ++kt, ++it) {
-          if (sm.abort_flag) { ok = false; break; }
-          const uint32_t b = it & 1u;
-          const uint32_t tph = (it >> 1) & 1u;
-          const int s = static_cast<int>(it % kStages);
-          const uint32_t ph = (it / kStages) & 1u;
-          // buffer b was drained (use it-2) and stage s holds K tile `it`
-          if (!mbar_wait(smem_u32(&sm.tempty[b]), tph ^ 1u) ||
-              !mbar_wait(smem_u32(&sm.full[s]), ph)) {
-            raise_abort(&sm.abort_flag);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sm.a[s]));
-          const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sm.b[s]));
-          const uint32_t d = tmem + b * BN;
+      // K tile it (counted across this CTA's output tiles) may start once
+      // its stage holds the operands (full) and its partial buffer it & 1
+      // has been drained (tempty).  The MMA queue holds little more than the
+      // running MMA, so a non-blocking test of the next stage goes between
+      // this K tile's MMAs, where it hides under a running one; the commit
+      // follows the last MMA at once (it starts the drain); the waits that
+      // may block (the drain, a stage that was not ready) come after it.
+      // No shared-memory flag is read per K tile: a shared-memory access
+      // right after a commit stalls this thread for a few hundred cycles,
+      // and the bounded waits catch an abort anyway.
+      const int my_tiles = unit < tiles ? (tiles - 1 - unit) / units + 1 : 0;
+      const uint32_t total = static_cast<uint32_t>(my_tiles) * static_cast<uint32_t>(KT);
+      bool ok = total == 0 ||
+                (mbar_wait(smem_u32(&sm.tempty[0]), 1u) && mbar_wait(smem_u32(&sm.full[0]), 0u));
+      if (!ok) raise_abort(&sm.abort_flag);
+      tc_fence_after();
+      for (uint32_t it = 0; it < total && ok; ++it) {
+        const uint32_t b = it & 1u;
+        const int s = static_cast<int>(it % kStages);
+        const bool more = it + 1 < total;
+        const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sm.a[s]));
+        const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sm.b[s]));
+        const uint32_t d = tmem + b * BN;
+        bool next_ready = false;
 #pragma unroll
-          for (int kk = 0; kk < BK / 32; ++kk) {
-            if (kPair)
-              mma_f8f6f4_pair(d, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : 0u);
-            else
-              mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : 0u);
-          }
+        for (int kk = 0; kk < BK / 32; ++kk) {
           if (kPair)
-            tc_commit_pair_mc(smem_u32(&sm.done[s]), 3);
+            mma_f8f6f4_pair(d, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : 0u);
           else
-            tc_commit(smem_u32(&sm.done[s]));
+            mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+          if (kk == 1 && more)
+            next_ready = mbar_test(smem_u32(&sm.full[(it + 1) % kStages]), ((it + 1) / kStages) & 1u);
         }
+        if (kPair)
+          tc_commit_pair_mc(smem_u32(&sm.done[s]), 3);
+        else
+          tc_commit(smem_u32(&sm.done[s]));
+        if (more && ((!next_ready && !mbar_wait(smem_u32(&sm.full[(it + 1) % kStages]),
+                                                ((it + 1) / kStages) & 1u)) ||
+                     !mbar_wait(smem_u32(&sm.tempty[(it + 1) & 1u]), (((it + 1) >> 1) & 1u) ^ 1u))) {
+          raise_abort(&sm.abort_flag);
+          ok = false;
+        }
+        tc_fence_after();
       }
       // every MMA this thread issued has completed once final_bar flips
       if (kPair)
@@ -626,11 +638,11 @@ int gemm_fp8_b_box_rows(bool pair) { return pair ? Cfg<true>::kBRows : Cfg<false
 
 bool gemm_fp8_use_pair(int M, int N, int num_sms) {
   // Pairs need an even SM count and enough 256 x 256 tiles to fill the GPU.
-  // Measured on the two large FP8 workloads the two shapes are within a few
-  // per cent of each other; the pair is taken for M >= N (it splits B, the
-  // smaller operand then, between the two CTAs), the single CTA otherwise.
+  // A pair moves two thirds of the single CTA's bytes per FLOP and keeps four
+  // stages in flight instead of three; on both large FP8 workloads it is the
+  // faster shape.
   const int64_t pair_tiles = (static_cast<int64_t>(M) + 255) / 256 * ((N + BN - 1) / BN);
-  return num_sms >= 2 && M >= N && pair_tiles >= num_sms / 2;
+  return num_sms >= 2 && pair_tiles >= num_sms / 2;
 }
 
 cudaError_t launch_gemm_fp8(const Fp8GemmArgs& a, int num_sms, cudaStream_t s) {
