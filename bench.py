@@ -549,6 +549,14 @@ def main():
                 "kernel": kernel,
                 "peak_source": f"{pk_kind} cuBLAS BF16 burst x {RATIO[dt]:g} (nominal dense "
                                f"{dt.upper()}:BF16 ratio)"}
+    if w.name != "decode":
+        # the tensor core's own rate for this kind, measured now on this GPU
+        # (outside the timed region): context beside the official peak
+        from fp4_gemm_gb300 import peak as mma_peak
+        kind = ("e2m1", True) if w.fp4 else (("e4m3", True) if w.mx8 else ("e4m3", False))
+        mp, _ = mma_peak.measure(kind[0], kind[1], False, 1 << 14, 5)
+        roof["mma_peak_microbench"] = mp
+        roof["frac_of_mma_peak_microbench"] = roof["achieved"] / mp
     metric, unit = w.metric()
     value = world * w.value_from_seconds(ms / 1e3)
     line = {
