@@ -32,7 +32,8 @@ LAYOUT = {"rowmajor": 0, "tcgen05": 1}
 
 EXPORTS = ("bsg_quantize_fp8", "bsg_quantize_mxfp4", "bsg_gemm", "bsg_gemm_workspace_size",
            "bsg_scale_bytes", "bsg_sf_to_tcgen05", "bsg_status_string", "bsg_device_error",
-           "bsg_num_sms", "bsg_gemm_decode_noalloc", "bsg_mma_peak", "bsg_quantize_mx")
+           "bsg_num_sms", "bsg_gemm_decode_noalloc", "bsg_mma_peak", "bsg_quantize_mx",
+           "bsg_mma_probe")
 
 
 class BsgError(RuntimeError):
@@ -78,6 +79,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsg_quantize_mx.argtypes = [vp, i32, i64, i64, i64, i32, f32, vp, vp, i32, vp]
     lib.bsg_quantize_mx.restype = i32
     lib.bsg_mma_peak.argtypes = [i32, i32, i32, i64, c.POINTER(i64), vp]
+    lib.bsg_mma_probe.argtypes = [vp, i32, vp, i32, vp, vp, vp]
+    lib.bsg_mma_probe.restype = i32
     lib.bsg_mma_peak.restype = i32
     _lib = lib
     return lib
@@ -127,6 +130,20 @@ def bsg_mma_peak(fmt: str = "e4m3", pair: bool = False, iters: int = 1 << 16,
     _check(load_library().bsg_mma_peak(FORMAT[fmt], bs, 1 if pair else 0, int(iters),
                                        ctypes.byref(flops), _stream(stream)), "bsg_mma_peak")
     return int(flops.value)
+
+
+def bsg_mma_probe(A: torch.Tensor, fa: str, B: torch.Tensor, fb: str, C: torch.Tensor,
+                  stream=None) -> torch.Tensor:
+    """One tcgen05.mma kind::f8f6f4: returns D (128, 16) float32 =
+    A (128, 32) . B (16, 32)^T + C (128, 16); A, B uint8 FP8 codes."""
+    if A.shape != (128, 32) or B.shape != (16, 32) or C.shape != (128, 16):
+        raise ValueError("bsg_mma_probe takes A (128, 32), B (16, 32), C (128, 16)")
+    A, B, C = A.contiguous(), B.contiguous(), C.contiguous().float()
+    D = torch.empty((128, 16), dtype=torch.float32, device=A.device)
+    _need_cuda(A, B, C, D)
+    _check(load_library().bsg_mma_probe(_ptr(A), FORMAT[fa], _ptr(B), FORMAT[fb], _ptr(C), _ptr(D),
+                                        _stream(stream)), "bsg_mma_probe")
+    return D
 
 
 def bsg_status_string(status: int) -> str:

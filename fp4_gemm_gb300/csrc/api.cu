@@ -324,14 +324,15 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
 bsg_status bsg_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return BSG_ERR_CUDA;
-  uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0, w4 = 0;
+  uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0, w4 = 0, w5 = 0;
   if (bsg::quantize_error_read_and_clear(s, &w0) != cudaSuccess ||
       bsg::gemm_fp8_error_read_and_clear(s, &w1) != cudaSuccess ||
       bsg::gemm_mxfp4_error_read_and_clear(s, &w2) != cudaSuccess ||
       bsg::mma_peak_error_read_and_clear(s, &w3) != cudaSuccess ||
-      bsg::gemm_mx_error_read_and_clear(s, &w4) != cudaSuccess)
+      bsg::gemm_mx_error_read_and_clear(s, &w4) != cudaSuccess ||
+      bsg::mma_probe_error_read_and_clear(s, &w5) != cudaSuccess)
     return BSG_ERR_CUDA;
-  const uint32_t w = w0 | w1 | w2 | w3 | w4;
+  const uint32_t w = w0 | w1 | w2 | w3 | w4 | w5;
   if (w & 1u) return BSG_ERR_TIMEOUT;
   if (w & 2u) return BSG_ERR_WORKSPACE;
   return BSG_OK;
@@ -352,6 +353,15 @@ bsg_status bsg_mma_peak(bsg_format fmt, int block_scaled, int pair, int64_t iter
   if (sms <= 0 || (pair && sms < 2)) return BSG_ERR_CUDA;
   return from_cuda(bsg::launch_mma_peak(kind, pair != 0, iters, sms,
                                         static_cast<cudaStream_t>(stream), flops));
+}
+
+bsg_status bsg_mma_probe(const uint8_t* A, bsg_format fa, const uint8_t* B, bsg_format fb,
+                         const float* C, float* D, void* stream) {
+  if (A == nullptr || B == nullptr || C == nullptr || D == nullptr) return BSG_ERR_INVALID_ARG;
+  if (!is_fp8(fa) || !is_fp8(fb)) return BSG_ERR_UNSUPPORTED;
+  if (!aligned(C, 4) || !aligned(D, 4)) return BSG_ERR_ALIGNMENT;
+  return from_cuda(bsg::launch_mma_probe(A, fa == BSG_E4M3 ? 0 : 1, B, fb == BSG_E4M3 ? 0 : 1, C, D,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -16,6 +16,7 @@ cudaError_t gemm_fp8_error_read_and_clear(cudaStream_t s, uint32_t* out);
 cudaError_t gemm_mxfp4_error_read_and_clear(cudaStream_t s, uint32_t* out);
 cudaError_t mma_peak_error_read_and_clear(cudaStream_t s, uint32_t* out);
 cudaError_t gemm_mx_error_read_and_clear(cudaStream_t s, uint32_t* out);
+cudaError_t mma_probe_error_read_and_clear(cudaStream_t s, uint32_t* out);
 
 // ------------------------------------------------------------- quantisers
 // src_bf16: source is BF16 (else FP32).  fmt: 0 E4M3, 1 E5M2.
@@ -111,5 +112,10 @@ cudaError_t launch_gemm_mxfp4_decode(const Mxfp4GemmArgs& a, int num_sms, cudaSt
 // 1 block-scaled FP8 (single CTA only), 2 block-scaled FP4.
 cudaError_t launch_mma_peak(int kind, bool pair, int64_t iters, int num_sms, cudaStream_t s,
                             int64_t* flops);
+
+// One tcgen05.mma kind::f8f6f4: D[128][16] = A[128][32] . B[16][32]^T + C
+// (row-major device arrays; fmt 0 E4M3, 1 E5M2).
+cudaError_t launch_mma_probe(const uint8_t* A, int afmt, const uint8_t* B, int bfmt, const float* C,
+                             float* D, cudaStream_t s);
 
 }  // namespace bsg

@@ -253,6 +253,26 @@ bsg_status bsg_gemm_decode_noalloc(int64_t M, int64_t N, int64_t K, const void* 
 bsg_status bsg_mma_peak(bsg_format fmt, int block_scaled, int pair, int64_t iters, int64_t* flops,
                         void* stream);
 
+/* bsg_mma_probe - one tensor-core MMA on given operands (verification only).
+ *
+ * "FP8 MMA internals on Hopper" shows that a single FP8 MMA instruction on
+ * H100 is not exact (products aligned to the largest exponent, bits more than
+ * 13 places below it dropped, the sum rounded toward zero to 13 fraction
+ * bits) and prints test vectors with the bits H100 returns; "Exact models of
+ * AMD matrix cores", section 3, models such units from test vectors and
+ * random campaigns.  This entry point is the instrument for the same question
+ * on this GPU: it runs exactly one tcgen05.mma kind::f8f6f4 (M128 N16 K32,
+ * FP32 accumulate) and returns its result:
+ *     D[128][16] = A[128][32] . B[16][32]^T + C[128][16]
+ * A, B    device, FP8 codes, row-major (B's rows are the N dimension, K
+ *         contiguous), formats fa / fb (BSG_E4M3 or BSG_E5M2).
+ * C, D    device, FP32, row-major 128 x 16 (C is the accumulator loaded into
+ *         tensor memory before the MMA).
+ * Errors: BSG_ERR_INVALID_ARG (null), BSG_ERR_UNSUPPORTED (non-FP8 format),
+ *         BSG_ERR_ALIGNMENT, BSG_ERR_CUDA. */
+bsg_status bsg_mma_probe(const uint8_t* A, bsg_format fa, const uint8_t* B, bsg_format fb,
+                         const float* C, float* D, void* stream);
+
 /* Human-readable name of a status. */
 const char* bsg_status_string(bsg_status status);
 

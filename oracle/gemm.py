@@ -131,3 +131,82 @@ def within_tolerance(D_gpu: np.ndarray, D_ref: np.ndarray, Bnd: np.ndarray,
         allowed = allowed + 8e-3 * np.abs(D_ref)
     ratio = err / allowed
     return bool(np.all(err <= allowed)), float(np.max(ratio)) if ratio.size else 0.0
+
+
+# --------------------------------------------------------------------------
+# Bit-level emulation of the promoted FP8 GEMM on a tensor core whose FP8 MMA
+# follows the fused dot-add model of "FP8 MMA internals on Hopper" (fda.py)
+# with GB300's measured parameters.  Per output element and 128-wide K tile
+# t: P_t is formed by the chain of MMAs over its 32-wide K blocks (the first
+# without an accumulator, each later one taking the previous result as c),
+# then promoted as acc = fma(fl32(s_A * s_B), P_t, acc) with one FP32
+# rounding; finally D = fl32(acc + C) and, for BF16 output, round to nearest
+# even.  This is the arithmetic the per-K-tile promotion of "FP8 GEMM on
+# CDNA4" section 4.4 and "FP8 MMA internals on Hopper" leads to, written
+# out step by step; it is exact where the GEMM is exact (see the tests).
+
+def _f32(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to FP32 (nearest even), kept as float64."""
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+def f32_fma(a: np.ndarray, b: np.ndarray, c: np.ndarray) -> np.ndarray:
+    """fl32(a * b + c) with a single rounding, for FP32 inputs.
+
+    a * b is exact in float64 (24 + 24 bits).  s = fl64(a*b + c) plus the
+    exact remainder e (Knuth's two-sum) is the exact result; rounding s to
+    FP32 can differ from rounding the exact value only when s is itself an
+    FP32 midpoint, and then e says which way the exact value lies."""
+    p = np.asarray(a, np.float64) * np.asarray(b, np.float64)
+    c = np.asarray(c, np.float64)
+    s = p + c
+    bv = s - p
+    av = s - bv
+    e = (p - av) + (c - bv)
+    r = _f32(s)
+    lo = np.where(r <= s, r, np.nextafter(r.astype(np.float32), np.float32(-np.inf)).astype(np.float64))
+    hi = np.where(r >= s, r, np.nextafter(r.astype(np.float32), np.float32(np.inf)).astype(np.float64))
+    mid = (s - lo == hi - s) & (lo != hi)
+    return np.where(mid & (e > 0), hi, np.where(mid & (e < 0), lo, r))
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """Round FP32 values to BF16 (nearest, ties to even), kept as float64."""
+    u = np.asarray(x, np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return (u.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def gemm_fp8_bits(A: np.ndarray, fa: str, sA: np.ndarray, ga: str,
+                  B: np.ndarray, fb: str, sB: np.ndarray, gb: str,
+                  rows, cols, C: np.ndarray | None = None, out: str = "f32",
+                  F: int | None = None, G: int | None = None) -> np.ndarray:
+    """Emulate the promoted FP8 GEMM bit for bit at the elements (rows[n],
+    cols[n]).  Arguments as gemm_fp8; returns float64 values (FP32, or BF16
+    for out="bf16")."""
+    from . import fda
+    F = fda.GB300_F if F is None else F
+    G = fda.GB300_G if G is None else G
+    rows = np.asarray(rows)
+    cols = np.asarray(cols)
+    if len(rows) > 4096:   # bounded working set: the elements are independent
+        return np.concatenate([gemm_fp8_bits(A, fa, sA, ga, B, fb, sB, gb, rows[i:i + 4096],
+                                             cols[i:i + 4096], C, out, F, G)
+                               for i in range(0, len(rows), 4096)])
+    K = A.shape[1]
+    Kp = -(-K // 32) * 32
+    a = np.zeros((len(rows), Kp))
+    b = np.zeros((len(cols), Kp))
+    a[:, :K] = formats.decode_array(A[rows], fa)
+    b[:, :K] = formats.decode_array(B[cols], fb)
+    acc = np.zeros(len(rows))
+    for t in range(_cdiv(K, TILE)):
+        P = np.zeros(len(rows))
+        for kb in range(t * TILE, min((t + 1) * TILE, Kp), 32):
+            P = fda.fda_batch(a[:, kb:kb + 32], b[:, kb:kb + 32], P, F=F, G=G)
+        sa = (sA[rows // TILE, t] if ga == "tile" else sA[t, rows]).astype(np.float64)
+        sb = (sB[cols // TILE, t] if gb == "tile" else sB[t, cols]).astype(np.float64)
+        acc = f32_fma(_f32(sa * sb), P, acc)
+    if C is not None:
+        acc = f32_fma(acc, np.ones_like(acc), np.asarray(C, np.float64)[rows, cols])
+    return bf16_round(acc) if out == "bf16" else acc
