@@ -18,6 +18,10 @@ Workloads (synthetic, seeded; see synth/):
               E8M0 scale per 32 along K, applied by the tensor core, so the
               GEMM needs no promotion): quantise the activations with the MX
               rule, then the block-scaled FP8 GEMM, BF16 out.
+  ffn_up_q8out  the FFN-up step with the quantiser fused into the GEMM's
+              epilogue: the output leaves as E4M3 codes with one FP32 scale
+              per 1x128 run of a row (the next GEMM's activation operand)
+              instead of BF16.  Same FLOPs; output bytes 1 + 4/128 per element.
 
 One JSON line is printed by rank 0.  Timing: W warm-up steps, then K steps.
 For the three full-size workloads every input and output exists in several
@@ -61,10 +65,10 @@ L2_BYTES = 129 << 20
 
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = {"fp8": ["gemm_fp8.cu", "common.cuh"], "fp4": ["gemm_mxfp4.cu", "common.cuh"],
+KERNEL_SOURCES = {"fp8": ["gemm_fp8.cu", "common.cuh", "quant_math.cuh"], "fp4": ["gemm_mxfp4.cu", "common.cuh"],
                   "mx8": ["gemm_mx.cu", "common.cuh"]}
 # workloads that reuse another workload's shape and seeded inputs
-SHAPE_OF = {"mxfp8_ffn_up": "ffn_up"}
+SHAPE_OF = {"mxfp8_ffn_up": "ffn_up", "ffn_up_q8out": "ffn_up"}
 
 
 def kernel_source_hash(files):
@@ -104,7 +108,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="ffn_up",
-                    choices=["ffn_up", "dgrad", "decode", "fp8_256", "mxfp4_1024", "mxfp8_ffn_up"])
+                    choices=["ffn_up", "dgrad", "decode", "fp8_256", "mxfp4_1024", "mxfp8_ffn_up",
+                             "ffn_up_q8out"])
     ap.add_argument("--m", type=int, default=None, help="override M (e.g. 1 for decode)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -128,8 +133,11 @@ class Workload:
         A, B = synth.make(src, m=M)
         self.fp4 = name in ("decode", "mxfp4_1024")
         self.mx8 = name == "mxfp8_ffn_up"
+        self.q8out = name == "ffn_up_q8out"
         if name == "ffn_up":
             self.fa, self.fb, self.ga, self.gb, self.out = "e4m3", "e4m3", "row", "tile", "bf16"
+        elif self.q8out:
+            self.fa, self.fb, self.ga, self.gb, self.out = "e4m3", "e4m3", "row", "tile", "e4m3/row"
         elif name == "dgrad":
             self.fa, self.fb, self.ga, self.gb, self.out = "e5m2", "e4m3", "tile", "tile", "f32"
         elif name == "fp8_256":
@@ -172,11 +180,16 @@ class Workload:
                 st["qa"], st["sa"] = bsg.bsg_quantize_mx(st["A"], self.fa, "tcgen05")
             else:
                 st["qa"], st["sa"] = bsg.bsg_quantize_fp8(st["A"], self.fa, self.ga)
-            st["D"] = torch.empty((M, N), dtype=torch.bfloat16 if self.out == "bf16" else torch.float32,
-                                  device=dev)
+            if self.q8out:
+                st["D"] = torch.empty((M, N), dtype=torch.uint8, device=dev)
+                st["sD"] = torch.empty(((N + 127) // 128, M), dtype=torch.float32, device=dev)
+            else:
+                st["D"] = torch.empty((M, N), dtype=torch.bfloat16 if self.out == "bf16" else torch.float32,
+                                      device=dev)
             self.sets.append(st)
         self.A, self.D = self.sets[0]["A"], self.sets[0]["D"]
         self.D_host = torch.empty_like(self.D, device="cpu").pin_memory()
+        self.sD_host = torch.empty_like(self.sets[0]["sD"], device="cpu").pin_memory() if self.q8out else None
         self.ws = bsg.workspace_for(M, N, K, self.fa, self.fb, dev)
         torch.cuda.synchronize()
 
@@ -191,6 +204,10 @@ class Workload:
 
     def gemm(self, r=0):
         st = self.sets[r]
+        if self.q8out:
+            self.bsg.bsg_gemm_quantized(st["qa"], self.fa, st["sa"], self.ga, st["qb"], self.fb, st["sb"],
+                                        self.gb, qfmt="e4m3", Dq=st["D"], sD=st["sD"])
+            return
         self.bsg.bsg_gemm(st["qa"], self.fa, st["sa"], self.ga, st["qb"], self.fb, st["sb"], self.gb,
                           out=self.out, D=st["D"], workspace=self.ws, K=self.K)
 
@@ -216,7 +233,10 @@ class Workload:
         else:
             a = M * K + (M * -(-K // 128) * 4 if self.ga == "row" else 4 * -(-M // 128) * -(-K // 128))
             b = N * K + 4 * -(-N // 128) * -(-K // 128)
-        d = M * N * (2 if self.out == "bf16" else 4)
+        if self.q8out:
+            d = M * N + 4 * M * -(-N // 128)
+        else:
+            d = M * N * (2 if self.out == "bf16" else 4)
         return a + b + d
 
     def step_bytes(self):
@@ -327,6 +347,20 @@ def cpu_baseline(name, m_override, target_s=15.0):
                 "kind": "oracle",
                 "sample": f"{name}: {rows} of {M} rows of A with {ncols} of {N} rows of B (K={K}); "
                           f"oracle MXFP8 quantise (both operands) + FP64 GEMM, {dt:.1f} s"}
+    if name == "ffn_up_q8out":
+        rows = 128
+        A, B = synth.make("ffn_up", m=rows)
+        t0 = time.perf_counter()
+        qa, sa = oq.quantize_fp8(A, "e4m3", "row")
+        qb, sb = oq.quantize_fp8(B, "e4m3", "tile")
+        D, _ = og.gemm_fp8(qa, "e4m3", sa, "row", qb, "e4m3", sb, "tile")
+        oq.quantize_fp8(D.astype(np.float32), "e4m3", "row")
+        dt = time.perf_counter() - t0
+        return {"value": 2.0 * rows * N * K / dt / 1e12, "unit": "TFLOP/s", "cores": cores,
+                "kind": "oracle",
+                "sample": f"{name}: {rows} of {M} rows of A with all of B (N={N}, K={K}); oracle "
+                          f"quantise (both operands) + FP64 GEMM + 1x128 quantiser of the output, "
+                          f"{dt:.1f} s"}
     fa, fb, ga, gb = {"ffn_up": ("e4m3", "e4m3", "row", "tile"),
                       "dgrad": ("e5m2", "e4m3", "tile", "tile"),
                       "fp8_256": ("e4m3", "e4m3", "tile", "tile"),
@@ -504,12 +538,16 @@ def main():
     if not args.no_e2e:
         h2d = w.A_host_t.numel() * w.A_host_t.element_size()
         d2h = w.D.numel() * w.D.element_size()
+        if w.q8out:
+            d2h += w.sD_host.numel() * w.sD_host.element_size()
 
         def e2e_step(i):
             st = w.sets[i % R]
             st["A"].copy_(w.A_host_t, non_blocking=True)
             w.step(i % R)
             w.D_host.copy_(st["D"], non_blocking=True)
+            if w.q8out:
+                w.sD_host.copy_(st["sD"], non_blocking=True)
 
         for i in range(2 * R):
             e2e_step(i)

@@ -33,7 +33,7 @@ LAYOUT = {"rowmajor": 0, "tcgen05": 1}
 EXPORTS = ("bsg_quantize_fp8", "bsg_quantize_mxfp4", "bsg_gemm", "bsg_gemm_workspace_size",
            "bsg_scale_bytes", "bsg_sf_to_tcgen05", "bsg_status_string", "bsg_device_error",
            "bsg_num_sms", "bsg_gemm_decode_noalloc", "bsg_mma_peak", "bsg_quantize_mx",
-           "bsg_mma_probe")
+           "bsg_mma_probe", "bsg_gemm_quantized")
 
 
 class BsgError(RuntimeError):
@@ -62,6 +62,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsg_quantize_mxfp4.restype = i32
     lib.bsg_gemm.argtypes = [i64, i64, i64, vp, i32, vp, i32, vp, i32, vp, i32, vp, vp, i32, vp, sz, vp]
     lib.bsg_gemm.restype = i32
+    lib.bsg_gemm_quantized.argtypes = [i64, i64, i64, vp, i32, vp, i32, vp, i32, vp, i32, vp, i32,
+                                       f32, vp, vp, vp]
+    lib.bsg_gemm_quantized.restype = i32
     lib.bsg_gemm_workspace_size.argtypes = [i64, i64, i64, i32, i32]
     lib.bsg_gemm_workspace_size.restype = sz
     lib.bsg_scale_bytes.argtypes = [i64, i64, i32, i32]
@@ -286,6 +289,28 @@ def bsg_gemm(A: torch.Tensor, fa: str, sA: torch.Tensor, ga: str,
                         0 if workspace is None else workspace.numel(), _stream(stream)),
            "bsg_gemm")
     return D
+
+
+def bsg_gemm_quantized(A: torch.Tensor, fa: str, sA: torch.Tensor, ga: str,
+                       B: torch.Tensor, fb: str, sB: torch.Tensor, gb: str,
+                       C: torch.Tensor | None = None, qfmt: str = "e4m3", fmt_max: float = 0.0,
+                       Dq: torch.Tensor | None = None, sD: torch.Tensor | None = None,
+                       stream=None):
+    """The FP8 GEMM with its result quantised per 1x128 run of a row in the
+    epilogue.  Returns (Dq (M, N) uint8 codes, sD (ceil(N/128), M) float32),
+    ready to be the activation operand of the next bsg_gemm with "row" scales."""
+    lib = load_library()
+    M, N, K = A.shape[0], B.shape[0], A.shape[1]
+    if Dq is None:
+        Dq = torch.empty((M, N), dtype=torch.uint8, device=A.device)
+    if sD is None:
+        sD = torch.empty(((N + 127) // 128, M), dtype=torch.float32, device=A.device)
+    _need_cuda(A, sA, B, sB, C, Dq, sD)
+    _check(lib.bsg_gemm_quantized(M, N, K, _ptr(A), FORMAT[fa], _ptr(sA), GRAN[ga], _ptr(B),
+                                  FORMAT[fb], _ptr(sB), GRAN[gb], _ptr(C), FORMAT[qfmt],
+                                  float(fmt_max), _ptr(Dq), _ptr(sD), _stream(stream)),
+           "bsg_gemm_quantized")
+    return Dq, sD
 
 
 def bsg_gemm_decode_noalloc(A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor, sB: torch.Tensor,

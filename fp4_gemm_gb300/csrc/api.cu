@@ -82,14 +82,15 @@ bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t inner_bytes, u
 
 bool make_out_map(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols, int elem_bytes) {
   EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr || (elem_bytes != 2 && elem_bytes != 4)) return false;
+  if (fn == nullptr || (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4)) return false;
   if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || (cols * elem_bytes) % 16 != 0) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * static_cast<uint64_t>(elem_bytes)};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem_bytes), 128};
   cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapDataType dt =
-      elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const CUtensorMapDataType dt = elem_bytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   return fn(map, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -112,6 +113,39 @@ bool make_kmajor_map_chunked(CUtensorMap* map, const void* base, uint64_t inner_
 }  // namespace bsg
 
 using bsg::make_kmajor_map;
+
+namespace {
+
+void fill_fp8_args(Fp8GemmArgs* a, int64_t M, int64_t N, int64_t K, bsg_format fa, const void* sA,
+                   bsg_scale_gran ga, bsg_format fb, const void* sB, bsg_scale_gran gb,
+                   const float* C) {
+  a->M = static_cast<int>(M);
+  a->N = static_cast<int>(N);
+  a->K = static_cast<int>(K);
+  a->afmt = fa == BSG_E4M3 ? 0 : 1;
+  a->bfmt = fb == BSG_E4M3 ? 0 : 1;
+  a->sA = static_cast<const float*>(sA);
+  a->a_row = ga == BSG_SCALE_ROW1x128;
+  a->sB = static_cast<const float*>(sB);
+  a->b_row = gb == BSG_SCALE_ROW1x128;
+  a->C = C;
+}
+
+// Shape choice, tensor maps and launch of the promoted FP8 GEMM; D (a->D)
+// is written by TMA stores when its base and row pitch allow.
+bsg_status run_fp8(Fp8GemmArgs* a, const void* A, const void* B, int out_elem_bytes, int sms,
+                   cudaStream_t s) {
+  a->pair = bsg::gemm_fp8_use_pair(a->M, a->N, sms);
+  a->tma_out = bsg::make_out_map(&a->tmD, a->D, static_cast<uint64_t>(a->M),
+                                 static_cast<uint64_t>(a->N), out_elem_bytes);
+  if (!make_kmajor_map(&a->tmA, A, a->K, a->M, a->K, 128) ||
+      !make_kmajor_map(&a->tmB, B, a->K, a->N, a->K,
+                       static_cast<uint32_t>(bsg::gemm_fp8_b_box_rows(a->pair))))
+    return BSG_ERR_CUDA;
+  return from_cuda(bsg::launch_gemm_fp8(*a, sms, s));
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -214,6 +248,40 @@ size_t bsg_gemm_workspace_size(int64_t M, int64_t N, int64_t K, bsg_format fa, b
   return 0;
 }
 
+
+bsg_status bsg_gemm_quantized(int64_t M, int64_t N, int64_t K, const void* A, bsg_format fa,
+                              const void* sA, bsg_scale_gran ga, const void* B, bsg_format fb,
+                              const void* sB, bsg_scale_gran gb, const float* C, bsg_format qfmt,
+                              float fmt_max, uint8_t* Dq, float* sD, void* stream) {
+  if (A == nullptr || B == nullptr || sA == nullptr || sB == nullptr || Dq == nullptr ||
+      sD == nullptr)
+    return BSG_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return BSG_ERR_INVALID_ARG;
+  if (!(fmt_max >= 0.0f) || !(fmt_max <= 0x1p64f)) return BSG_ERR_INVALID_ARG;
+  if (fa < BSG_E4M3 || fa > BSG_E2M1 || fb < BSG_E4M3 || fb > BSG_E2M1) return BSG_ERR_INVALID_ARG;
+  if (qfmt < BSG_E4M3 || qfmt > BSG_E2M1) return BSG_ERR_INVALID_ARG;
+  if (!is_fp8(fa) || !is_fp8(fb) || !is_fp8(qfmt)) return BSG_ERR_UNSUPPORTED;
+  if (ga != BSG_SCALE_TILE128x128 && ga != BSG_SCALE_ROW1x128) return BSG_ERR_UNSUPPORTED;
+  if (gb != BSG_SCALE_TILE128x128 && gb != BSG_SCALE_ROW1x128) return BSG_ERR_UNSUPPORTED;
+  if (K % 16) return BSG_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sA, 4) || !aligned(sB, 4) || !aligned(sD, 4) ||
+      (C != nullptr && !aligned(C, 4)))
+    return BSG_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int sms = num_sms_current();
+  if (sms <= 0) return BSG_ERR_CUDA;
+  Fp8GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  fill_fp8_args(&a, M, N, K, fa, sA, ga, fb, sB, gb, C);
+  a.D = Dq;
+  a.out_fp8 = true;
+  a.qfmt = qfmt == BSG_E4M3 ? 0 : 1;
+  a.qmax = fmt_max != 0.0f ? fmt_max : (qfmt == BSG_E4M3 ? 448.0f : 57344.0f);
+  a.sD = sD;
+  return run_fp8(&a, A, B, 1, sms, s);
+}
+
 bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format fa, const void* sA,
                     bsg_scale_gran ga, const void* B, bsg_format fb, const void* sB,
                     bsg_scale_gran gb, const float* C, void* D, bsg_dtype out, void* workspace,
@@ -271,25 +339,10 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
   if (fp8) {
     Fp8GemmArgs a;
     std::memset(&a, 0, sizeof(a));
-    a.M = static_cast<int>(M);
-    a.N = static_cast<int>(N);
-    a.K = static_cast<int>(K);
-    a.afmt = fa == BSG_E4M3 ? 0 : 1;
-    a.bfmt = fb == BSG_E4M3 ? 0 : 1;
-    a.sA = static_cast<const float*>(sA);
-    a.a_row = ga == BSG_SCALE_ROW1x128;
-    a.sB = static_cast<const float*>(sB);
-    a.b_row = gb == BSG_SCALE_ROW1x128;
-    a.C = C;
+    fill_fp8_args(&a, M, N, K, fa, sA, ga, fb, sB, gb, C);
     a.D = D;
     a.out_bf16 = out == BSG_BF16;
-    a.pair = bsg::gemm_fp8_use_pair(a.M, a.N, sms);
-    a.tma_out = bsg::make_out_map(&a.tmD, D, static_cast<uint64_t>(M), static_cast<uint64_t>(N),
-                                  out == BSG_BF16 ? 2 : 4);
-    if (!make_kmajor_map(&a.tmA, A, K, M, K, 128) ||
-        !make_kmajor_map(&a.tmB, B, K, N, K, static_cast<uint32_t>(bsg::gemm_fp8_b_box_rows(a.pair))))
-      return BSG_ERR_CUDA;
-    return from_cuda(bsg::launch_gemm_fp8(a, sms, s));
+    return run_fp8(&a, A, B, out == BSG_BF16 ? 2 : 4, sms, s);
   }
   {
     Mxfp4GemmArgs a;

@@ -52,6 +52,7 @@
 // CTA-wide abort flag and all roles unwind to the final barrier.
 #include "common.cuh"
 #include "kernels.h"
+#include "quant_math.cuh"
 
 namespace bsg {
 namespace {
@@ -85,6 +86,11 @@ __device__ __forceinline__ void tmem_wait_cols(uint32_t (&r)[W]) {
   if constexpr (W == 32) tc_wait_ld_32(r); else tc_wait_ld_16(r);
 }
 
+// What the epilogue writes: FP32, BF16 (round to nearest even), or the
+// result quantised to E4M3 / E5M2 per 1 x 128 run of a row (codes + FP32
+// scales)
+enum OutKind : int { kOutF32 = 0, kOutBF16 = 1, kOutE4M3 = 2, kOutE5M2 = 3 };
+
 constexpr uint32_t kOutBytes = 64 * 1024;   // output staging
 constexpr uint32_t kOutBlock = 128 * 128;   // one 128-row x 128-byte swizzled box
 
@@ -102,8 +108,8 @@ template <bool kPair>
 struct __align__(1024) Smem {
   uint8_t a[Cfg<kPair>::kStages][BM * BK];
   uint8_t b[Cfg<kPair>::kStages][Cfg<kPair>::kBRows * BK];
-  // finished tile on its way to D: BF16 -> the two column halves in two
-  // 32 KB slots; FP32 -> one half at a time in all 64 KB
+  // finished tile on its way to D: BF16 / FP8 codes -> the two column
+  // halves in two 32 KB slots; FP32 -> one half at a time in all 64 KB
   uint8_t out[kOutBytes];
   float sa[kScaleSlots][BM];
   float sb[kScaleSlots][BN];
@@ -140,18 +146,60 @@ __device__ __forceinline__ TileCoord tile_coord(int t, int num_m, int num_n, boo
   return along_n ? TileCoord{i, o} : TileCoord{o, i};
 }
 
+// ---- the fused output quantiser (one thread = one 1 x 128 run of a row) --
+//
+// Codes of the 128 values (64 pairs) of acc divided by s, correctly rounded
+// to FP32 first (as the stand-alone quantiser and the 1 x 128 rule require),
+// then RNE-satfinite to the FP8 format, staged as eight 16-byte pieces of
+// the 128-byte-swizzled box.  The quotient is Markstein's division (see
+// GroupDiv): q0 = x r, q1 = q0 + (x - q0 s) r, q2 = q1 + (x - q1 s) r, valid
+// for s in [2^-80, 2^80] (the caller scales other groups into that range).
+// Scalar FMAs: the paired form needs aligned register pairs, and with the
+// 128 accumulators live that made the promotion warps spill.  A code's sign bit is
+// taken from x: a non-zero quotient of x by a positive s has x's sign, and a
+// quotient that rounds to zero is -0 exactly when x is negative.
+template <int kFmt>
+__device__ __forceinline__ void stage_codes(const uint64_t (&acc)[64], float s, float r,
+                                                 uint32_t base, int row) {
+  const uint64_t r2 = f32x2_pack(r, r);
+  const uint64_t ns2 = f32x2_pack(-s, -s);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint32_t w[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const uint64_t x01 = acc[8 * c + 2 * p], x23 = acc[8 * c + 2 * p + 1];
+      float v[4], q[4];
+      f32x2_unpack(x01, v[0], v[1]);
+      f32x2_unpack(x23, v[2], v[3]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float t = v[i] * r;
+        t = fmaf(fmaf(-t, s, v[i]), r, t);
+        q[i] = fmaf(fmaf(-t, s, v[i]), r, t);
+      }
+      const float a = q[0], b = q[1], cc = q[2], d = q[3];
+      const uint32_t sg = __byte_perm(
+          __byte_perm(static_cast<uint32_t>(x01), static_cast<uint32_t>(x01 >> 32), 0x0073),
+          __byte_perm(static_cast<uint32_t>(x23), static_cast<uint32_t>(x23 >> 32), 0x0073), 0x5410);
+      w[p] = (cvt4_fp8(kFmt, a, b, cc, d) & 0x7F7F7F7Fu) | (sg & 0x80808080u);
+    }
+    st_shared_v4(base + row * 128 + ((c ^ (row & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
+  }
+}
+
 __device__ __forceinline__ void raise_abort(volatile uint32_t* flag) {
   atomicOr(&g_fp8_error, kErrTimeout);
   *flag = 1u;
 }
 
-template <bool kPair, bool kARow, bool kBRow, bool kBF16Out>
+template <bool kPair, bool kARow, bool kBRow, int kOut>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD, const float* __restrict__ sA,
                     const float* __restrict__ sB, const float* __restrict__ Cin,
-                    void* __restrict__ Dout, int M, int N, int K, uint32_t idesc, bool tma_out,
-                    bool raster_n) {
+                    void* __restrict__ Dout, float* __restrict__ sD, int M, int N, int K,
+                    uint32_t idesc, bool tma_out, bool raster_n, float qmax) {
   using C = Cfg<kPair>;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -358,7 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kStoreWarp) {
     // -------------------------------------------------------- output store
     setmaxnreg_dec<kRegsSmall>();
-    constexpr int kElem = kBF16Out ? 2 : 4;
+    constexpr bool kCodes = kOut == kOutE4M3 || kOut == kOutE5M2;
+    constexpr int kElem = kOut == kOutF32 ? 4 : (kOut == kOutBF16 ? 2 : 1);
     constexpr int kBoxCols = 128 / kElem;              // columns of one swizzled box
     constexpr int kHalfBlocks = 128 / kBoxCols;        // boxes of a 128-column half
     const uint64_t stream_out = l2_policy_evict_first();   // D is not re-read here
@@ -376,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         good = __shfl_sync(0xffffffffu, good, 0);
         if (!good) { ok = false; break; }
-        const uint32_t base = smem_u32(sm.out) + (kBF16Out ? h * (kOutBytes / 2) : 0u);
+        const uint32_t base = smem_u32(sm.out) + (kOut != kOutF32 ? h * (kOutBytes / 2) : 0u);
         const int col0 = tc.n * BN + h * 128;
         if (tma_out) {
           if (lane == 0) {
@@ -403,7 +452,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < kPerPiece; ++j) {
               if (col + j >= N) break;
-              if (kBF16Out)
+              if (kCodes)
+                reinterpret_cast<uint8_t*>(Dout)[grow * N + col + j] =
+                    static_cast<uint8_t>(w[j / 4] >> (8 * (j % 4)));
+              else if (kOut == kOutBF16)
                 reinterpret_cast<uint16_t*>(Dout)[grow * N + col + j] =
                     static_cast<uint16_t>(w[j / 2] >> (16 * (j % 2)));
               else
@@ -493,46 +545,103 @@ __global__ void __launch_bounds__(kThreads, 1)
       // buffer as 16-byte pieces in the 128-byte-swizzled box layout (piece
       // c of row r at r*128 + ((c ^ (r & 7)) << 4) inside its box), which
       // the TMA store reads and which spreads a warp's 32 rows over all
-      // banks.  BF16: half g owns slot g and waits for the store of its own
-      // previous tile; FP32: a half fills the whole buffer, so half 0 waits
-      // for the previous tile's half 1 and half 1 for this tile's half 0.
+      // banks.  BF16 / FP8: half g owns slot g and waits for the store of its
+      // own previous tile; FP32: a half fills the whole buffer, so half 0
+      // waits for the previous tile's half 1 and half 1 for this tile's half 0.
       {
-        constexpr int kElem = kBF16Out ? 2 : 4;
-        constexpr int kPerPiece = 16 / kElem;
-        const uint32_t wb = kBF16Out ? static_cast<uint32_t>(g) : static_cast<uint32_t>(g ^ 1);
-        const uint32_t wph = kBF16Out ? ((tl & 1u) ^ 1u) : (g == 0 ? ((tl & 1u) ^ 1u) : (tl & 1u));
+        constexpr bool kSlots = kOut != kOutF32;
+        const uint32_t wb = kSlots ? static_cast<uint32_t>(g) : static_cast<uint32_t>(g ^ 1);
+        const uint32_t wph = kSlots ? ((tl & 1u) ^ 1u) : (g == 0 ? ((tl & 1u) ^ 1u) : (tl & 1u));
         if (!mbar_wait(smem_u32(&sm.ofree[wb]), wph)) {
           raise_abort(&sm.abort_flag);
           break;
         }
-        const uint32_t base = smem_u32(sm.out) + (kBF16Out ? g * (kOutBytes / 2) : 0u);
+        const uint32_t base = smem_u32(sm.out) + (kSlots ? g * (kOutBytes / 2) : 0u);
         const int64_t grow = static_cast<int64_t>(tc.m) * C::kTileM + rank * BM + row;
         const int gcol0 = tc.n * BN + g * 128;
-#pragma unroll
-        for (int c = 0; c < 128 / kPerPiece; ++c) {
-          float v[kPerPiece];
-#pragma unroll
-          for (int j = 0; j < kPerPiece / 2; ++j)
-            f32x2_unpack(acc[(c * kPerPiece) / 2 + j], v[2 * j], v[2 * j + 1]);
+        if constexpr (kOut == kOutE4M3 || kOut == kOutE5M2) {
+          // The fused quantiser: this thread's 128 columns are one 1 x 128
+          // run of the output row, i.e. one scale group of the next GEMM's
+          // activations, so the group maximum needs no exchange between
+          // threads.  Same rule as the stand-alone quantiser: s = max|x| /
+          // fmt_max (1 if 0), codes = RNE_satfinite(x / s) with a correctly
+          // rounded division.  Columns at or beyond N are zeroed first.
+          const int nvalid = N - gcol0;
           if (Cin != nullptr && grow < M) {
 #pragma unroll
-            for (int j = 0; j < kPerPiece; ++j) {
-              const int col = gcol0 + c * kPerPiece + j;
-              if (col < N) v[j] += __ldg(Cin + grow * N + col);
+            for (int j = 0; j < 64; ++j) {
+              float x0, x1;
+              f32x2_unpack(acc[j], x0, x1);
+              if (2 * j < nvalid) x0 += __ldg(Cin + grow * N + gcol0 + 2 * j);
+              if (2 * j + 1 < nvalid) x1 += __ldg(Cin + grow * N + gcol0 + 2 * j + 1);
+              acc[j] = f32x2_pack(x0, x1);
             }
           }
-          uint4 u;
-          if (kBF16Out) {
-            u.x = pack_bf16x2(v[0], v[1]);
-            u.y = pack_bf16x2(v[2], v[3]);
-            u.z = pack_bf16x2(v[4 % kPerPiece], v[5 % kPerPiece]);
-            u.w = pack_bf16x2(v[6 % kPerPiece], v[7 % kPerPiece]);
-          } else {
-            u = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
-                           __float_as_uint(v[2 % kPerPiece]), __float_as_uint(v[3 % kPerPiece]));
+          if (nvalid < 128) {    // the group crosses N: zero what lies beyond
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+              float x0, x1;
+              f32x2_unpack(acc[j], x0, x1);
+              acc[j] = f32x2_pack(2 * j < nvalid ? x0 : 0.0f, 2 * j + 1 < nvalid ? x1 : 0.0f);
+            }
           }
-          const int blk = c / 8, cc = c % 8;
-          st_shared_v4(base + blk * kOutBlock + row * 128 + ((cc ^ (row & 7)) << 4), u);
+          float m[8];            // eight independent max chains
+#pragma unroll
+          for (int j = 0; j < 8; ++j) m[j] = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            float x0, x1;
+            f32x2_unpack(acc[j], x0, x1);
+            m[j & 7] = fmaxf(m[j & 7], fmaxf(fabsf(x0), fabsf(x1)));
+          }
+          const float amax = fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])),
+                                   fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+          const float sc = fp8_scale(amax, qmax);
+          float sd = sc;         // the divisor the quotients are formed with
+          if (!(sc >= 0x1p-80f && sc <= 0x1p80f)) {
+            // Bring s into the division's range with a power of two P applied
+            // to s and to every x: x / s is unchanged.  P = 2^100 (s < 2^-80)
+            // is exact for all x (|x| <= s fmt_max < 2^-16 with fmt_max <=
+            // 2^64).  P = 2^-100 (s > 2^80) rounds x only when |x| < 2^-26,
+            // i.e. |x / s| < 2^-106, which is a signed zero in FP8 either way.
+            const float P = sc < 0x1p-80f ? 0x1p100f : 0x1p-100f;
+            const uint64_t P2 = f32x2_pack(P, P);
+#pragma unroll
+            for (int j = 0; j < 64; ++j) acc[j] = fmul2(acc[j], P2);
+            sd = sc * P;
+          }
+          stage_codes<kOut == kOutE4M3 ? 0 : 1>(acc, sd, __frcp_rn(sd), base, row);
+          // scales K-tile major for the next GEMM: [ceil(N/128)][M]
+          if (grow < M && nvalid > 0) sD[static_cast<int64_t>(gcol0 / 128) * M + grow] = sc;
+        } else {
+          constexpr int kElem = kOut == kOutBF16 ? 2 : 4;
+          constexpr int kPerPiece = 16 / kElem;
+#pragma unroll
+          for (int c = 0; c < 128 / kPerPiece; ++c) {
+            float v[kPerPiece];
+#pragma unroll
+            for (int j = 0; j < kPerPiece / 2; ++j)
+              f32x2_unpack(acc[(c * kPerPiece) / 2 + j], v[2 * j], v[2 * j + 1]);
+            if (Cin != nullptr && grow < M) {
+#pragma unroll
+              for (int j = 0; j < kPerPiece; ++j) {
+                const int col = gcol0 + c * kPerPiece + j;
+                if (col < N) v[j] += __ldg(Cin + grow * N + col);
+              }
+            }
+            uint4 u;
+            if (kOut == kOutBF16) {
+              u.x = pack_bf16x2(v[0], v[1]);
+              u.y = pack_bf16x2(v[2], v[3]);
+              u.z = pack_bf16x2(v[4 % kPerPiece], v[5 % kPerPiece]);
+              u.w = pack_bf16x2(v[6 % kPerPiece], v[7 % kPerPiece]);
+            } else {
+              u = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
+                             __float_as_uint(v[2 % kPerPiece]), __float_as_uint(v[3 % kPerPiece]));
+            }
+            const int blk = c / 8, cc = c % 8;
+            st_shared_v4(base + blk * kOutBlock + row * 128 + ((cc ^ (row & 7)) << 4), u);
+          }
         }
         fence_proxy_async_smem();    // the staged bytes are read by the TMA (async proxy)
         __syncwarp();
@@ -557,9 +666,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool kPair, bool kARow, bool kBRow, bool kBF16Out>
+template <bool kPair, bool kARow, bool kBRow, int kOut>
 cudaError_t launch_variant(const Fp8GemmArgs& a, int num_sms, cudaStream_t s) {
-  auto kern = gemm_fp8_kernel<kPair, kARow, kBRow, kBF16Out>;
+  auto kern = gemm_fp8_kernel<kPair, kARow, kBRow, kOut>;
   const size_t smem = sizeof(Smem<kPair>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
@@ -603,23 +712,26 @@ cudaError_t launch_variant(const Fp8GemmArgs& a, int num_sms, cudaStream_t s) {
   const bool raster_n = static_cast<int64_t>(a.M) < static_cast<int64_t>(a.N);
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmD, a.sA, a.sB, a.C, a.D, a.M, a.N, a.K,
-                            idesc, tma_out, raster_n);
+  return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmD, a.sA, a.sB, a.C, a.D, a.sD, a.M, a.N,
+                            a.K, idesc, tma_out, raster_n, a.qmax);
+}
+
+template <bool kPair, int kOut>
+cudaError_t launch_grans(const Fp8GemmArgs& a, int num_sms, cudaStream_t s) {
+  if (a.a_row)
+    return a.b_row ? launch_variant<kPair, true, true, kOut>(a, num_sms, s)
+                   : launch_variant<kPair, true, false, kOut>(a, num_sms, s);
+  return a.b_row ? launch_variant<kPair, false, true, kOut>(a, num_sms, s)
+                 : launch_variant<kPair, false, false, kOut>(a, num_sms, s);
 }
 
 template <bool kPair>
 cudaError_t launch_shape(const Fp8GemmArgs& a, int num_sms, cudaStream_t s) {
-  const int key = (a.a_row ? 4 : 0) | (a.b_row ? 2 : 0) | (a.out_bf16 ? 1 : 0);
-  switch (key) {
-    case 0: return launch_variant<kPair, false, false, false>(a, num_sms, s);
-    case 1: return launch_variant<kPair, false, false, true>(a, num_sms, s);
-    case 2: return launch_variant<kPair, false, true, false>(a, num_sms, s);
-    case 3: return launch_variant<kPair, false, true, true>(a, num_sms, s);
-    case 4: return launch_variant<kPair, true, false, false>(a, num_sms, s);
-    case 5: return launch_variant<kPair, true, false, true>(a, num_sms, s);
-    case 6: return launch_variant<kPair, true, true, false>(a, num_sms, s);
-    default: return launch_variant<kPair, true, true, true>(a, num_sms, s);
-  }
+  if (a.out_fp8)
+    return a.qfmt == 0 ? launch_grans<kPair, kOutE4M3>(a, num_sms, s)
+                       : launch_grans<kPair, kOutE5M2>(a, num_sms, s);
+  return a.out_bf16 ? launch_grans<kPair, kOutBF16>(a, num_sms, s)
+                    : launch_grans<kPair, kOutF32>(a, num_sms, s);
 }
 
 }  // namespace

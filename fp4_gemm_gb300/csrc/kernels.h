@@ -61,8 +61,12 @@ struct Fp8GemmArgs {
   const float* sB;
   bool b_row;
   const float* C;            // optional FP32 addend
-  void* D;
+  void* D;                   // FP32 / BF16 values, or FP8 codes when out_fp8
   bool out_bf16;
+  bool out_fp8;              // quantise the result per 1x128 run of a row
+  int qfmt;                  // out_fp8: 0 E4M3, 1 E5M2
+  float qmax;                // out_fp8: the value a group's maximum maps to
+  float* sD;                 // out_fp8: FP32 scales [ceil(N/128)][M]
   bool pair;                 // CTA-pair kernel (256 x 256 tiles, tcgen05 cta_group::2)
   bool tma_out;              // tmD is valid: D is written by TMA tensor stores
   CUtensorMap tmA, tmB;      // K-major operand maps (box 128 B x rows)

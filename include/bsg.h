@@ -197,6 +197,38 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K,
                     const float* C, void* D, bsg_dtype out,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* bsg_gemm_quantized - the promoted FP8 GEMM with its output quantised in
+ * the epilogue (a quantiser fused into the producing GEMM).
+ *
+ * Computes R = sum_k (s_A a_k)(s_B b_k) + C exactly as bsg_gemm does with FP8
+ * operands and FP32 scales (FP32 result before any output rounding), then
+ * quantises R the way bsg_quantize_fp8 does with BSG_SCALE_ROW1x128 ("FP8
+ * GEMM on CDNA4" section 3.3, the online scale of the next GEMM's
+ * activations; "Rubin FP4 GEMM deep dive" section 4.2 step 4, activations
+ * quantised at run time): for each 1 x 128 run G of a row of R,
+ *     s_G = max_{x in G} |x| / fmt_max   (FP32, round to nearest; 1.0 if 0)
+ *     q   = RNE_satfinite_qfmt(x / s_G)  (IEEE FP32 division)
+ * so Dq and sD can be passed straight to bsg_gemm as an activation operand
+ * with BSG_SCALE_ROW1x128 scales (K = N of this call).
+ *
+ * A, fa, sA, ga, B, fb, sB, gb, C  as bsg_gemm, FP8 operands with FP32 scales
+ *          (BSG_SCALE_TILE128x128 or BSG_SCALE_ROW1x128) only.
+ * qfmt     BSG_E4M3 or BSG_E5M2.
+ * fmt_max  the value a group's maximum maps to; 0 selects the format's own
+ *          maximum (448 / 57344).  Must be in [0, 2^64].
+ * Dq       device, M x N codes, leading dimension N bytes (TMA stores when Dq
+ *          is 16-byte aligned and N % 16 == 0, a bounds-checked copy else).
+ * sD       device, FP32 scales [ceil(N/128)][M] (4-byte aligned).
+ * Constraints: M, N, K > 0, K % 16 == 0; A, B 16-byte aligned.
+ * Errors: BSG_ERR_INVALID_ARG, BSG_ERR_UNSUPPORTED (non-FP8 operands, E8M0
+ *         scales or qfmt), BSG_ERR_ALIGNMENT, BSG_ERR_CUDA.
+ */
+bsg_status bsg_gemm_quantized(int64_t M, int64_t N, int64_t K,
+                              const void* A, bsg_format fa, const void* sA, bsg_scale_gran ga,
+                              const void* B, bsg_format fb, const void* sB, bsg_scale_gran gb,
+                              const float* C, bsg_format qfmt, float fmt_max,
+                              uint8_t* Dq, float* sD, void* stream);
+
 /* Bytes of device workspace bsg_gemm needs for this problem (0 if none). */
 size_t bsg_gemm_workspace_size(int64_t M, int64_t N, int64_t K, bsg_format fa, bsg_format fb);
 
