@@ -120,6 +120,34 @@ def gemm_mxfp8(A: np.ndarray, fa: str, sfA: np.ndarray, B: np.ndarray, fb: str, 
     return D, Bnd
 
 
+def nvfp4_values(packed: np.ndarray, sf: np.ndarray) -> np.ndarray:
+    """Real values E4M3(sf) * a of a packed NVFP4 matrix (rows x K) with
+    row-major E4M3 block scales (rows x K/16), exact in FP64; the tensor scale
+    is not included (the GEMM applies g_A * g_B as alpha)."""
+    codes = formats.unpack_e2m1(packed)
+    vals = formats.decode_array(codes, "e2m1")
+    scale = formats.decode_array(sf, "e4m3")
+    R, K = vals.shape
+    return (vals.reshape(R, K // 16, 16) * scale[:, :, None]).reshape(R, K)
+
+
+def gemm_nvfp4(A: np.ndarray, sfA: np.ndarray, B: np.ndarray, sfB: np.ndarray,
+               alpha: float = 1.0, C: np.ndarray | None = None, rows=None):
+    """NVFP4 GEMM: D = alpha * sum_k (sa a_k)(sb b_k) + C with A packed
+    M x K/2, sfA M x K/16, B packed N x K/2, sfB N x K/16 (E4M3 scales,
+    row-major); alpha = g_A * g_B.  Returns (D, Bnd) in FP64."""
+    M = A.shape[0]
+    ri = np.arange(M) if rows is None else np.asarray(rows)
+    a = nvfp4_values(A[ri], sfA[ri])
+    b = nvfp4_values(B, sfB)
+    al = float(np.float32(alpha))
+    D = al * (a @ b.T)
+    Bnd = abs(al) * (np.abs(a) @ np.abs(b).T)
+    if C is not None:
+        D += np.asarray(C, dtype=np.float64)[ri]
+    return D, Bnd
+
+
 def within_tolerance(D_gpu: np.ndarray, D_ref: np.ndarray, Bnd: np.ndarray,
                      bf16: bool = False):
     """Elementwise check of |D_gpu - D_ref| <= 1e-4 * Bnd + 1e-6, plus

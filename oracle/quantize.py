@@ -20,6 +20,17 @@ MXFP8 quantiser - the same MX rule (§2.2: 32 elements along K share one E8M0
   pages give the rule for E2M1 only; taking it unchanged for FP8 elements is a
   reading (the "smaller formats share the block structure" of §2.2).
 
+NVFP4 quantiser - "Rubin FP4 GEMM deep dive", §5.3 (smaller blocks, 16
+  elements, give finer scales at twice the scale storage) and §2.2 (the block
+  scale is kept in a higher-precision format such as FP8): per block of 16
+  elements along K, v = max_abs / 6 (FP32), the scale code is v / g rounded to
+  E4M3 (RNE, saturating at 448; g is an FP32 tensor scale, 1 by default, that
+  keeps v / g inside E4M3's range), the block's scale is s = fl32(E4M3(code)
+  * g), and each element is RNE_satfinite_E2M1(fl32(x / s)); a block whose s
+  is 0 stores all-zero codes.  The tensor scale g is not on the pages: it is
+  the reading that lets an E4M3 scale cover data of any magnitude (the
+  dynamic-range concern of §3.2); the GEMM multiplies its sum by g_A * g_B.
+
 Readings where the pages leave a step open (also listed in the design notes):
   * the scale is s = max_abs / fmt_max computed in FP32 with round-to-nearest,
     and the element is q = RNE_satfinite(x / s) with an IEEE FP32 division
@@ -41,6 +52,7 @@ from . import formats
 
 TILE = 128        # FP8 scale tile along both dimensions (and along K for 1x128)
 MX_BLOCK = 32     # MXFP4 block along K
+NV_BLOCK = 16     # NVFP4 block along K
 
 
 def _cdiv(a: int, b: int) -> int:
@@ -162,17 +174,43 @@ def quantize_mxfp8(x: np.ndarray, fmt: str, fmt_max: float | None = None):
     return codes.astype(np.uint8), sf
 
 
-def sf_to_tcgen05_layout(sf: np.ndarray) -> np.ndarray:
+def quantize_nvfp4(x: np.ndarray, tensor_scale: float = 1.0):
+    """Quantise a row-major float32 matrix (rows x K, K % 16 == 0) to NVFP4:
+    E2M1 elements, one E4M3 scale per 16 elements along K, an FP32 tensor
+    scale g.  Returns (packed uint8 R x K/2, sf uint8 R x K/16 E4M3 codes)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    R, K = x.shape
+    if K % NV_BLOCK:
+        raise ValueError("K must be a multiple of 16")
+    g = np.float32(tensor_scale)
+    if not (np.isfinite(g) and g > 0):
+        raise ValueError("tensor_scale must be positive and finite")
+    nb = K // NV_BLOCK
+    blocks = x.reshape(R, nb, NV_BLOCK)
+    amax = np.max(np.abs(blocks), axis=2)
+    v = amax / np.float32(6.0)                          # FP32, round to nearest
+    u = v / g                                           # FP32, round to nearest
+    sf = formats.encode(u, "e4m3").astype(np.uint8)     # RNE, saturating at 448
+    s = (formats.decode_array(sf, "e4m3").astype(np.float32) * g).astype(np.float32)
+    safe = np.where(s == 0, np.float32(1.0), s)
+    q = (blocks / safe[:, :, None]).astype(np.float32)  # IEEE FP32 division
+    codes = formats.encode(q.reshape(R, K), "e2m1").reshape(R, nb, NV_BLOCK)
+    codes[s == 0] = 0
+    return formats.pack_e2m1(codes.reshape(R, K).astype(np.uint8)), sf
+
+
+def sf_to_tcgen05_layout(sf: np.ndarray, pad: int = 127) -> np.ndarray:
     """Rearrange row-major E8M0 scales [R][KB] into the storage order the
     block-scaled tensor-core MMA reads them in (not from the pages; NVIDIA's
     documented 128-row x 4-scale atom): atoms of 512 bytes, ordered by
     (row block of 128, group of 4 K-blocks); inside an atom the byte of row r,
     K-block c is at (r % 32) * 16 + ((r % 128) // 32) * 4 + (c % 4).
-    Padding bytes (rows beyond R, K-blocks beyond KB) hold code 127.
+    Padding bytes (rows beyond R, K-blocks beyond KB) hold `pad`: 127 (E8M0
+    1.0) for E8M0 scales, 0 for E4M3 scales.
     """
     R, KB = sf.shape
     rb, cb = _cdiv(R, 128), _cdiv(KB, 4)
-    out = np.full(rb * cb * 512, 127, dtype=np.uint8)
+    out = np.full(rb * cb * 512, pad, dtype=np.uint8)
     r = np.arange(R)[:, None]
     c = np.arange(KB)[None, :]
     off = ((r // 128) * cb + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + (c % 4)

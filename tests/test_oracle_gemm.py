@@ -261,3 +261,41 @@ def test_emulated_gemm_truncates_far_terms():
     assert d[0] == 257.0
     D, _ = gemm.gemm_fp8(A, "e4m3", one, "tile", B, "e4m3", one, "tile")
     assert D[0, 0] == 257.0 + 2.0 ** -18
+
+
+def test_nvfp4_brute_force_tiny():
+    g = np.random.default_rng(9)
+    M, N, K = 3, 5, 64
+    xa = (g.standard_normal((M, K)) * np.exp2(g.uniform(-3, 3, (M, 1)))).astype(np.float32)
+    xb = (g.standard_normal((N, K)) * 0.02).astype(np.float32)
+    A, sfA = quantize.quantize_nvfp4(xa)
+    B, sfB = quantize.quantize_nvfp4(xb, tensor_scale=2.0 ** -6)
+    C = g.standard_normal((M, N)).astype(np.float32)
+    alpha = 2.0 ** -6
+    D, Bnd = gemm.gemm_nvfp4(A, sfA, B, sfB, alpha=alpha, C=C)
+    ca, cb = formats.unpack_e2m1(A), formats.unpack_e2m1(B)
+    for i in range(M):
+        for j in range(N):
+            acc = Fraction(0)
+            bnd = Fraction(0)
+            for k in range(K):
+                ta = Fraction(formats.decode_e2m1(int(ca[i, k]))) * Fraction(formats.decode_e4m3(int(sfA[i, k // 16])))
+                tb = Fraction(formats.decode_e2m1(int(cb[j, k]))) * Fraction(formats.decode_e4m3(int(sfB[j, k // 16])))
+                acc += ta * tb
+                bnd += abs(ta * tb)
+            exact = Fraction(alpha) * acc + Fraction(float(C[i, j]))
+            assert abs(D[i, j] - float(exact)) <= 1e-15 * float(bnd * Fraction(alpha)) + 1e-300
+            assert Bnd[i, j] == pytest.approx(float(Fraction(alpha) * bnd), rel=1e-15)
+
+
+def test_nvfp4_closed_form_with_mixed_block_scales():
+    # every element 1.0 (E2M1 code 2), A's scales 2.0 (E4M3 0x40) on the
+    # first 16-block and 0.5 (0x30) elsewhere, B's scales 1.0 (0x38), alpha 3
+    M, N, K = 2, 3, 64
+    A = formats.pack_e2m1(np.full((M, K), 2, np.uint8))
+    B = formats.pack_e2m1(np.full((N, K), 2, np.uint8))
+    sfA = np.full((M, K // 16), 0x30, np.uint8)
+    sfA[:, 0] = 0x40
+    sfB = np.full((N, K // 16), 0x38, np.uint8)
+    D, _ = gemm.gemm_nvfp4(A, sfA, B, sfB, alpha=3.0)
+    assert np.all(D == 3.0 * (16 * 2.0 + 48 * 0.5))

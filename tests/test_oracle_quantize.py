@@ -198,3 +198,89 @@ def test_mxfp8_zero_block_and_sizes():
     codes, sf = quantize.quantize_mxfp8(x, "e4m3")
     assert codes.shape == (2, K) and sf.shape == (2, K // int(FACTS["mx_block"]))
     assert (sf[0] == 127).all() and (codes[0] == 0).all()
+
+
+# ------------------------------------------------------------------ NVFP4
+def _nv_block(vals):
+    x = np.zeros((1, 16), np.float32)
+    x[0, :len(vals)] = vals
+    return x
+
+
+def _nv_codes(packed):
+    return formats.unpack_e2m1(packed)[0]
+
+
+def test_nvfp4_hand_worked_unit_scale():
+    # max 6 -> v = 1 -> E4M3 1.0 (0x38), s = 1: elements rounded directly,
+    # ties to the even E2M1 code (1.25 -> 1, 5 -> 4, 0.25 -> 0, 0.75 -> 1)
+    x = _nv_block([6, -3, 1.25, 5, 0.25, 0.75, -0.75, 2.5, 3.5])
+    p, sf = quantize.quantize_nvfp4(x)
+    assert sf[0, 0] == 0x38
+    vals = formats.decode_array(_nv_codes(p), "e2m1")[:9]
+    assert list(vals) == [6, -3, 1, 4, 0, 1, -1, 2, 4]
+
+
+def test_nvfp4_scale_rounds_to_e4m3_and_elements_divide():
+    # max 7: v = 7/6 = 1.1666..; the E4M3 neighbours are 1.125 and 1.25, so
+    # the scale is 1.125 (0x39); 7 / 1.125 = 6.22 saturates to 6;
+    # 2.8125 / 1.125 = 2.5 ties to 2 (even), 3.375 / 1.125 = 3
+    x = _nv_block([7, 2.8125, -3.375])
+    p, sf = quantize.quantize_nvfp4(x)
+    assert sf[0, 0] == 0x39
+    vals = formats.decode_array(_nv_codes(p), "e2m1")[:3]
+    assert list(vals) == [6, 2, -3]
+
+
+def test_nvfp4_scale_saturates_and_subnormal_scales():
+    # max 6000: v = 1000 > 448 -> scale 448 (0x7E); 6000 / 448 saturates to 6
+    p, sf = quantize.quantize_nvfp4(_nv_block([6000, 896]))
+    assert sf[0, 0] == 0x7E
+    assert list(formats.decode_array(_nv_codes(p), "e2m1")[:2]) == [6, 2]
+    # max 0.006: v = 0.001 lies between E4M3 subnormals 0 and 2^-9 (nearer
+    # 2^-9) -> code 0x01; 0.006 / 2^-9 = 3.07 -> 3
+    p, sf = quantize.quantize_nvfp4(_nv_block([0.006]))
+    assert sf[0, 0] == 0x01
+    assert formats.decode_array(_nv_codes(p), "e2m1")[0] == 3
+
+
+def test_nvfp4_zero_and_underflowing_blocks():
+    x = np.zeros((2, 32), np.float32)
+    x[1, 16:] = 1e-5              # v = 1.7e-6 rounds to E4M3 zero: s = 0
+    x[1, 0] = 0.5
+    p, sf = quantize.quantize_nvfp4(x)
+    assert sf.shape == (2, 2) and p.shape == (2, 16)
+    assert sf[0, 0] == 0 and sf[0, 1] == 0 and sf[1, 1] == 0
+    codes = formats.unpack_e2m1(p)
+    assert not codes[0].any() and not codes[1, 16:].any()
+    assert formats.decode_array(codes[1, :1], "e2m1")[0] == 6   # 0.5 / (0.5/6 -> E4M3) = 6
+
+
+def test_nvfp4_tensor_scale_is_a_power_of_two_shift():
+    # with g = 2^-7 every block scale code equals the g = 1 code of x * 2^7,
+    # and the element codes are identical (all steps scale exactly)
+    g = np.random.default_rng(3)
+    x = (g.standard_normal((16, 128)) * 0.02).astype(np.float32)
+    p1, sf1 = quantize.quantize_nvfp4(x, tensor_scale=2.0 ** -7)
+    p2, sf2 = quantize.quantize_nvfp4(x * np.float32(2.0 ** 7))
+    assert np.array_equal(p1, p2) and np.array_equal(sf1, sf2)
+
+
+def test_nvfp4_reconstruction_bound():
+    g = np.random.default_rng(4)
+    x = (g.standard_normal((64, 256)) * np.exp2(g.uniform(-4, 4, (64, 1)))).astype(np.float32)
+    p, sf = quantize.quantize_nvfp4(x, tensor_scale=2.0 ** -3)
+    vals = formats.decode_array(formats.unpack_e2m1(p), "e2m1").reshape(64, 16, 16)
+    s = (formats.decode_array(sf, "e4m3") * 2.0 ** -3)[:, :, None]
+    blocks = x.reshape(64, 16, 16).astype(np.float64)
+    amax = np.max(np.abs(blocks), axis=2, keepdims=True)
+    # E2M1 steps are at most 2 (4 -> 6): error <= s; a scale rounded down by
+    # up to 1/16 can push the maximum past 6 s by at most amax / 16
+    assert np.all(np.abs(blocks - vals * s) <= s + amax / 16 + 1e-30)
+
+
+def test_tcgen05_layout_pad_byte():
+    sf = np.arange(5 * 3, dtype=np.uint8).reshape(5, 3) + 1
+    out = quantize.sf_to_tcgen05_layout(sf, pad=0)
+    assert out.size == 512 and np.count_nonzero(out) == 15
+    assert sorted(out[out != 0]) == sorted(sf.ravel())
