@@ -27,13 +27,13 @@ STATUS = {0: "BSG_OK", 1: "BSG_ERR_INVALID_ARG", 2: "BSG_ERR_UNSUPPORTED", 3: "B
           4: "BSG_ERR_CUDA", 5: "BSG_ERR_TIMEOUT", 6: "BSG_ERR_WORKSPACE"}
 FORMAT = {"e4m3": 0, "e5m2": 1, "e2m1": 2}
 DTYPE = {"f32": 0, "bf16": 1}
-GRAN = {"tile": 0, "row": 1, "mx": 2}
+GRAN = {"tile": 0, "row": 1, "mx": 2, "nv": 3}
 LAYOUT = {"rowmajor": 0, "tcgen05": 1}
 
 EXPORTS = ("bsg_quantize_fp8", "bsg_quantize_mxfp4", "bsg_gemm", "bsg_gemm_workspace_size",
            "bsg_scale_bytes", "bsg_sf_to_tcgen05", "bsg_status_string", "bsg_device_error",
            "bsg_num_sms", "bsg_gemm_decode_noalloc", "bsg_mma_peak", "bsg_quantize_mx",
-           "bsg_mma_probe", "bsg_gemm_quantized")
+           "bsg_mma_probe", "bsg_gemm_quantized", "bsg_quantize_nvfp4", "bsg_gemm_nvfp4")
 
 
 class BsgError(RuntimeError):
@@ -81,6 +81,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsg_gemm_decode_noalloc.restype = i32
     lib.bsg_quantize_mx.argtypes = [vp, i32, i64, i64, i64, i32, f32, vp, vp, i32, vp]
     lib.bsg_quantize_mx.restype = i32
+    lib.bsg_quantize_nvfp4.argtypes = [vp, i32, i64, i64, i64, f32, vp, vp, i32, vp]
+    lib.bsg_quantize_nvfp4.restype = i32
+    lib.bsg_gemm_nvfp4.argtypes = [i64, i64, i64, vp, vp, vp, vp, f32, vp, vp, i32, vp]
+    lib.bsg_gemm_nvfp4.restype = i32
     lib.bsg_mma_peak.argtypes = [i32, i32, i32, i64, c.POINTER(i64), vp]
     lib.bsg_mma_probe.argtypes = [vp, i32, vp, i32, vp, vp, vp]
     lib.bsg_mma_probe.restype = i32
@@ -234,6 +238,50 @@ def bsg_quantize_mx(x: torch.Tensor, fmt: str = "e4m3", layout: str = "tcgen05",
                                _ptr(q), _ptr(sf), LAYOUT[layout], _stream(stream)),
            "bsg_quantize_mx")
     return q, sf
+
+
+def bsg_quantize_nvfp4(x: torch.Tensor, layout: str = "tcgen05", tensor_scale: float = 1.0,
+                       q: torch.Tensor | None = None, sf: torch.Tensor | None = None, stream=None):
+    """NVFP4 quantisation, x: (rows, K) FP32 or BF16 CUDA tensor, K % 16 == 0.
+    Returns (packed E2M1 uint8 (rows, K/2), E4M3 scales): "rowmajor" scales
+    are (rows, K/16), "tcgen05" scales a flat buffer in the MMA's atom order."""
+    lib = load_library()
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D tensor with unit column stride")
+    rows, cols = x.shape
+    src = {torch.float32: 0, torch.bfloat16: 1}[x.dtype]
+    if q is None:
+        q = torch.empty((rows, cols // 2), dtype=torch.uint8, device=x.device)
+    if sf is None:
+        if layout == "rowmajor":
+            sf = torch.empty((rows, cols // 16), dtype=torch.uint8, device=x.device)
+        else:
+            n = lib.bsg_scale_bytes(rows, cols, GRAN["nv"], LAYOUT["tcgen05"])
+            sf = torch.empty((max(int(n), 1),), dtype=torch.uint8, device=x.device)
+    _need_cuda(x, q, sf)
+    _check(lib.bsg_quantize_nvfp4(_ptr(x), src, rows, cols, x.stride(0), float(tensor_scale),
+                                  _ptr(q), _ptr(sf), LAYOUT[layout], _stream(stream)),
+           "bsg_quantize_nvfp4")
+    return q, sf
+
+
+def bsg_gemm_nvfp4(A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor, sB: torch.Tensor,
+                   alpha: float = 1.0, C: torch.Tensor | None = None, out: str = "f32",
+                   D: torch.Tensor | None = None, K: int | None = None, stream=None):
+    """D = alpha * sum_k (s_A a_k)(s_B b_k) + C for NVFP4 operands: A (M, K/2)
+    and B (N, K/2) packed, sA / sB E4M3 scales in the tcgen05 layout."""
+    lib = load_library()
+    M, N = A.shape[0], B.shape[0]
+    if K is None:
+        K = A.shape[1] * 2
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.float32 if out == "f32" else torch.bfloat16,
+                        device=A.device)
+    _need_cuda(A, sA, B, sB, C, D)
+    _check(lib.bsg_gemm_nvfp4(M, N, K, _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), float(alpha), _ptr(C),
+                              _ptr(D), DTYPE[out], _stream(stream)),
+           "bsg_gemm_nvfp4")
+    return D
 
 
 def bsg_sf_to_tcgen05(sf_rowmajor: torch.Tensor, out: torch.Tensor | None = None, stream=None):

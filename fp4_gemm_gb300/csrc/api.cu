@@ -176,6 +176,11 @@ size_t bsg_scale_bytes(int64_t rows, int64_t cols, bsg_scale_gran gran, bsg_sf_l
       if (layout == BSG_SF_TCGEN05)
         return static_cast<size_t>(cdiv(rows, 128) * cdiv(cols / 32, 4) * 512);
       return static_cast<size_t>(rows * (cols / 32));
+    case BSG_SCALE_BLOCK1x16_E4M3:
+      if (cols % 16) return 0;
+      if (layout == BSG_SF_TCGEN05)
+        return static_cast<size_t>(cdiv(rows, 128) * cdiv(cols / 16, 4) * 512);
+      return static_cast<size_t>(rows * (cols / 16));
   }
   return 0;
 }
@@ -310,7 +315,9 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
     if (K % 16) return BSG_ERR_INVALID_ARG;
     if (!aligned(sA, 4) || !aligned(sB, 4)) return BSG_ERR_ALIGNMENT;
   } else {
-    if (ga != BSG_SCALE_BLOCK1x32_E8M0 || gb != BSG_SCALE_BLOCK1x32_E8M0) return BSG_ERR_UNSUPPORTED;
+    const bool mx = ga == BSG_SCALE_BLOCK1x32_E8M0 && gb == BSG_SCALE_BLOCK1x32_E8M0;
+    const bool nv = ga == BSG_SCALE_BLOCK1x16_E4M3 && gb == BSG_SCALE_BLOCK1x16_E4M3;
+    if (!mx && !nv) return BSG_ERR_UNSUPPORTED;
     if (K % 32) return BSG_ERR_INVALID_ARG;
     if (!aligned(sA, 16) || !aligned(sB, 16)) return BSG_ERR_ALIGNMENT;
   }
@@ -359,7 +366,12 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
     a.workspace_bytes = workspace_bytes;
     a.A = A;
     a.B = B;
-    if (M <= kDecodeMaxM) {
+    if (ga == BSG_SCALE_BLOCK1x16_E4M3) {
+      // NVFP4: the general kernel at every M, tensor scales folded into alpha
+      // by bsg_gemm_nvfp4 (1 here)
+      a.nvfp4 = true;
+      a.alpha = 1.0f;
+    } else if (M <= kDecodeMaxM) {
       const size_t need = bsg::gemm_mxfp4_decode_workspace(a.M, a.N, a.K, sms);
       if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)))
         return BSG_ERR_WORKSPACE;
@@ -372,6 +384,57 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
       return BSG_ERR_CUDA;
     return from_cuda(bsg::launch_gemm_mxfp4(a, sms, s));
   }
+}
+
+bsg_status bsg_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const void* A, const void* sA,
+                          const void* B, const void* sB, float alpha, const float* C, void* D,
+                          bsg_dtype out, void* stream) {
+  if (A == nullptr || B == nullptr || sA == nullptr || sB == nullptr || D == nullptr)
+    return BSG_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || K % 32)
+    return BSG_ERR_INVALID_ARG;
+  if (out != BSG_F32 && out != BSG_BF16) return BSG_ERR_INVALID_ARG;
+  if (!std::isfinite(alpha)) return BSG_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(sA, 16) || !aligned(sB, 16))
+    return BSG_ERR_ALIGNMENT;
+  if (!aligned(D, out == BSG_F32 ? 4 : 2) || (C != nullptr && !aligned(C, 4)))
+    return BSG_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int sms = num_sms_current();
+  if (sms <= 0) return BSG_ERR_CUDA;
+  Mxfp4GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.nvfp4 = true;
+  a.alpha = alpha;
+  a.sfA = static_cast<const uint8_t*>(sA);
+  a.sfB = static_cast<const uint8_t*>(sB);
+  a.C = C;
+  a.D = D;
+  a.out_bf16 = out == BSG_BF16;
+  a.A = A;
+  a.B = B;
+  if (!make_kmajor_map(&a.tmA, A, K / 2, M, K / 2, 128) ||
+      !make_kmajor_map(&a.tmB, B, K / 2, N, K / 2, 128))
+    return BSG_ERR_CUDA;
+  return from_cuda(bsg::launch_gemm_mxfp4(a, sms, s));
+}
+
+bsg_status bsg_quantize_nvfp4(const void* x, bsg_dtype src, int64_t rows, int64_t cols, int64_t ld,
+                              float tensor_scale, uint8_t* q_packed, uint8_t* sf,
+                              bsg_sf_layout layout, void* stream) {
+  if (x == nullptr || q_packed == nullptr || sf == nullptr) return BSG_ERR_INVALID_ARG;
+  if (rows <= 0 || cols <= 0 || ld < cols || rows > kMaxDim || cols > kMaxDim || cols % 16)
+    return BSG_ERR_INVALID_ARG;
+  if (src != BSG_F32 && src != BSG_BF16) return BSG_ERR_INVALID_ARG;
+  if (layout != BSG_SF_ROWMAJOR && layout != BSG_SF_TCGEN05) return BSG_ERR_INVALID_ARG;
+  if (!(tensor_scale >= 0x1p-126f) || !std::isfinite(tensor_scale)) return BSG_ERR_INVALID_ARG;
+  if (!aligned(x, src == BSG_F32 ? 4 : 2) || !aligned(q_packed, 4)) return BSG_ERR_ALIGNMENT;
+  return from_cuda(bsg::launch_quantize_nvfp4(x, src == BSG_BF16, rows, cols, ld, tensor_scale,
+                                              q_packed, sf, layout == BSG_SF_TCGEN05,
+                                              static_cast<cudaStream_t>(stream)));
 }
 
 bsg_status bsg_device_error(void* stream) {

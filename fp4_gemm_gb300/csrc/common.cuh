@@ -401,6 +401,20 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// NVFP4 MMA: E2M1 operands, one UE4M3 scale per 16 K per row (scale_vec::4X:
+// K = 64 per instruction, the four scale bytes of a row in one 32-bit tensor-
+// memory cell).
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Block-scaled FP8 MMA: E4M3 / E5M2 operands, one UE8M0 scale per 32 K per
 // row (scale_vec::1X: K = 32 per instruction, so one scale byte per row,
 // selected by the scale-factor ids of the instruction descriptor).
@@ -564,6 +578,15 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N, uint32
          | (1u << 23)               // scale type UE8M0
          | ((M >> 4) << 24)         // M / 16
          | (sfa_id << 29);          // A scale-factor id
+}
+
+// Instruction descriptor for kind::mxf4nvf4 with UE4M3 scales (NVFP4): E2M1
+// operands, scale type bit clear, scale-factor ids 0 (scale_vec::4X reads a
+// whole 32-bit cell).
+__host__ __device__ constexpr uint32_t idesc_nvf4(uint32_t M, uint32_t N) {
+  return (1u << 7) | (1u << 10)     // A, B = E2M1
+         | ((N >> 3) << 17)         // N / 8
+         | ((M >> 4) << 24);        // M / 16
 }
 
 // Instruction descriptor for kind::mxf8f6f4 block-scaled MMA: FP8 operands

@@ -56,15 +56,27 @@ constexpr int kStages = 5;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kTmemCols = 512;
-constexpr int kSfColsPerStage = 16;     // SFA: 2 atoms x 4 cols, SFB: 2 atoms x 4 cols
 constexpr int kSfBase = 2 * BN;         // after the two accumulators
 constexpr int kGroupM = 8;
 
+// A stage covers 256 K: MXFP4 (blocks of 32) needs 2 scale atoms per operand,
+// NVFP4 (blocks of 16) 4.  Each atom takes 4 tensor-memory columns; a stage's
+// columns hold A's atoms, then B's: 16 (MXFP4) or 32 (NVFP4) per stage, so
+// 5 stages fit beside the two accumulators in 512 columns.
+template <bool kNv>
+struct Fmt {
+  static constexpr int kAtoms = kNv ? 4 : 2;
+  static constexpr int kBlock = kNv ? 16 : 32;
+  static constexpr int kSfColsPerStage = 8 * kAtoms;
+};
+static_assert(kSfBase + kStages * Fmt<true>::kSfColsPerStage <= kTmemCols, "TMEM columns");
+
+template <bool kNv>
 struct __align__(1024) Smem {
   uint8_t a[kStages][BM * kRowBytes];
   uint8_t b[kStages][BN * kRowBytes];
-  uint8_t sfa[kStages][2 * kSfAtom];
-  uint8_t sfb[kStages][2 * kSfAtom];
+  uint8_t sfa[kStages][Fmt<kNv>::kAtoms * kSfAtom];
+  uint8_t sfb[kStages][Fmt<kNv>::kAtoms * kSfAtom];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t tfull[2];
@@ -84,15 +96,19 @@ __device__ __forceinline__ void tile_coord(int t, int num_m, int num_n, int& m, 
   n = local / gsz;
 }
 
-template <bool kBF16Out>
+// kNv: NVFP4 (UE4M3 scales per 16, kind::mxf4nvf4 scale_vec::4X) instead of
+// MXFP4 (UE8M0 per 32, kind::mxf4 scale_vec::2X); the sum is multiplied by
+// alpha (the product of the two tensor scales) before the addend.
+template <bool kBF16Out, bool kNv>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mxfp4_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const uint8_t* __restrict__ sfA,
                       const uint8_t* __restrict__ sfB, const float* __restrict__ Cin,
-                      void* __restrict__ Dout, int M, int N, int K, bool vec_out) {
+                      void* __restrict__ Dout, int M, int N, int K, bool vec_out, float alpha) {
+  using F = Fmt<kNv>;
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                      ~static_cast<uintptr_t>(1023));
+  Smem<kNv>& sm = *reinterpret_cast<Smem<kNv>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
   const int num_m = (M + BM - 1) / BM;
@@ -100,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tiles = num_m * num_n;
   const int kbytes = K / 2;
   const int KS = (kbytes + kRowBytes - 1) / kRowBytes;   // stages of 256 K
-  const int KA = (K / 32 + 3) / 4;                       // scale atoms along K
+  const int KA = (K / F::kBlock + 3) / 4;                // scale atoms along K
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -146,8 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const int ka0 = 2 * ks;
-          const int na = min(2, KA - ka0);
+          const int ka0 = F::kAtoms * ks;
+          const int na = min(F::kAtoms, KA - ka0);
           const uint32_t fb = smem_u32(&sm.full[s]);
           mbar_arrive_expect_tx(fb, (BM + BN) * kRowBytes + 2 * na * kSfAtom);
           tma_load_2d(smem_u32(sm.a[s]), &tmA, fb, ks * kRowBytes, m * BM);
@@ -183,21 +199,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const int ka0 = 2 * ks;
-          const int na = min(2, KA - ka0);
-          const uint32_t sfc = tmem + kSfBase + s * kSfColsPerStage;
+          const int ka0 = F::kAtoms * ks;
+          const int na = min(F::kAtoms, KA - ka0);
+          const uint32_t sfc = tmem + kSfBase + s * F::kSfColsPerStage;
+          const uint32_t sfbc = sfc + 4 * F::kAtoms;    // B's atoms follow A's
           for (int a = 0; a < na; ++a) {
             tc_cp_32x128b_warpx4(sfc + 4 * a, sdesc_sf_32x16(smem_u32(sm.sfa[s] + a * kSfAtom)));
-            tc_cp_32x128b_warpx4(sfc + 8 + 4 * a, sdesc_sf_32x16(smem_u32(sm.sfb[s] + a * kSfAtom)));
+            tc_cp_32x128b_warpx4(sfbc + 4 * a, sdesc_sf_32x16(smem_u32(sm.sfb[s] + a * kSfAtom)));
           }
           const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sm.a[s]));
           const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sm.b[s]));
           const int rem = kbytes - ks * kRowBytes;
           const int nk = min(4, (rem + 31) / 32);
           for (int kk = 0; kk < nk; ++kk) {
-            const uint32_t id = idesc_mxf4(BM, BN, (kk & 1) * 2, (kk & 1) * 2);
-            mma_mxf4(d, ad + 2 * kk, bd + 2 * kk, id, sfc + 4 * (kk >> 1), sfc + 8 + 4 * (kk >> 1),
-                     (ks > 0 || kk > 0) ? 1u : 0u);
+            const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
+            if (kNv) {
+              // K = 64 = one atom (4 blocks of 16) per MMA
+              mma_nvf4(d, ad + 2 * kk, bd + 2 * kk, idesc_nvf4(BM, BN), sfc + 4 * kk, sfbc + 4 * kk,
+                       acc);
+            } else {
+              // K = 64 = half an atom: the scale id picks bytes 0-1 or 2-3
+              const uint32_t id = idesc_mxf4(BM, BN, (kk & 1) * 2, (kk & 1) * 2);
+              mma_mxf4(d, ad + 2 * kk, bd + 2 * kk, id, sfc + 4 * (kk >> 1), sfbc + 4 * (kk >> 1),
+                       acc);
+            }
           }
           tc_commit(smem_u32(&sm.empty[s]));
         }
@@ -236,6 +261,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+          if (kNv) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] *= alpha;
+          }
           if (Cin != nullptr) {
 #pragma unroll
             for (int j = 0; j < 16; ++j)
@@ -742,16 +771,17 @@ cudaError_t gemm_mxfp4_error_read_and_clear(cudaStream_t s, uint32_t* out) {
 
 cudaError_t launch_gemm_mxfp4(const Mxfp4GemmArgs& a, int num_sms, cudaStream_t s) {
   using namespace general;
-  const size_t smem = sizeof(Smem) + 1024;
+  const size_t smem = (a.nvfp4 ? sizeof(Smem<true>) : sizeof(Smem<false>)) + 1024;
   const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
   const bool vec_out = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) &&
                        (a.out_bf16 ? (a.N % 8 == 0) : (a.N % 4 == 0));
-  auto kern = a.out_bf16 ? gemm_mxfp4_kernel<true> : gemm_mxfp4_kernel<false>;
+  auto kern = a.nvfp4 ? (a.out_bf16 ? gemm_mxfp4_kernel<true, true> : gemm_mxfp4_kernel<false, true>)
+                      : (a.out_bf16 ? gemm_mxfp4_kernel<true, false> : gemm_mxfp4_kernel<false, false>);
   const cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a.tmA, a.tmB, a.sfA, a.sfB, a.C, a.D,
-                    a.M, a.N, a.K, vec_out);
+                    a.M, a.N, a.K, vec_out, a.nvfp4 ? a.alpha : 1.0f);
 }
 
 size_t gemm_mxfp4_decode_workspace(int M, int N, int K, int num_sms) {

@@ -33,6 +33,11 @@ cudaError_t launch_quantize_fp8_row(const void* x, bool src_bf16, int64_t rows, 
 cudaError_t launch_quantize_mx(const void* x, bool src_bf16, int64_t rows, int64_t cols,
                                int64_t ld, int fmt, float fmt_max, uint8_t* q, uint8_t* sf,
                                bool tc_layout, cudaStream_t s);
+// NVFP4: E2M1 codes, one E4M3 scale per 16 along K (row-major or tcgen05
+// layout, padding 0), FP32 tensor scale g.
+cudaError_t launch_quantize_nvfp4(const void* x, bool src_bf16, int64_t rows, int64_t cols,
+                                  int64_t ld, float tensor_scale, uint8_t* q, uint8_t* sf,
+                                  bool tc_layout, cudaStream_t s);
 cudaError_t launch_sf_to_tcgen05(const uint8_t* sf, int64_t rows, int64_t kblocks, uint8_t* out,
                                  cudaStream_t s);
 
@@ -93,6 +98,8 @@ cudaError_t launch_gemm_mx(const MxGemmArgs& a, int num_sms, cudaStream_t s);
 
 struct Mxfp4GemmArgs {
   int M, N, K;
+  bool nvfp4;                // E4M3 scales per 16 (general kernel only)
+  float alpha;               // nvfp4: the sum is multiplied by alpha
   const uint8_t* sfA;        // tcgen05 layout
   const uint8_t* sfB;
   const float* C;

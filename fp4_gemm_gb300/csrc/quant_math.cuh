@@ -76,6 +76,12 @@ __device__ __forceinline__ uint32_t e8m0_nearest(float v) {
   return static_cast<uint32_t>(e < 0 ? 0 : (e > 254 ? 254 : e));
 }
 
+// Value of a non-negative E4M3 code (0x00..0x7E), exact in FP32.
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  return e != 0u ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : static_cast<float>(m) * 0x1p-9f;
+}
+
 __device__ __forceinline__ uint32_t cvt2_e2m1(float first, float second) {
   uint32_t r;
   asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}\n"

@@ -253,6 +253,63 @@ __global__ void __launch_bounds__(256) quantize_mx_kernel(
   }
 }
 
+// NVFP4 quantiser: one warp per (row, 256-column chunk = 16 blocks of 16);
+// lane l owns 8 elements, 2 lanes per block.  Per block: v = max / 6,
+// u = v / g (FP32 divisions, round to nearest), scale code = E4M3(u)
+// (RNE, saturating), s = E4M3(code) * g, elements E2M1(x / s) with a
+// correctly rounded quotient; s = 0 stores zero codes.  In the tcgen05
+// layout the padding bytes get 0.
+template <bool kBF16, bool kTC>
+__global__ void __launch_bounds__(256) quantize_nvfp4_kernel(
+    const void* __restrict__ x, int64_t rows, int64_t cols, int64_t ld, float g, bool vec_in,
+    uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  grid_dep_launch();
+  grid_dep_wait();
+  const int64_t kb = cols / 16;
+  const int64_t kb_pad = kTC ? ((kb + 3) / 4) * 4 : kb;
+  const int64_t chunks = (kb_pad + 15) / 16;
+  const int64_t rows_pad = kTC ? ((rows + 127) / 128) * 128 : rows;
+  const int64_t w = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (w >= rows_pad * chunks) return;
+  const int64_t row = w / chunks, chunk = w % chunks;
+  const int lane = threadIdx.x & 31;
+  const int64_t b = chunk * 16 + (lane >> 1);
+  const int64_t col = b * 16 + (lane & 1) * 8;
+  const bool data = row < rows && b < kb;
+  float v[8];
+  if (data) {
+    load4<kBF16>(x, row, col, cols, ld, vec_in, *reinterpret_cast<float(*)[4]>(&v[0]));
+    load4<kBF16>(x, row, col + 4, cols, ld, vec_in, *reinterpret_cast<float(*)[4]>(&v[4]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  const float u = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
+  const uint32_t code = cvt4_fp8(0, u, 0.0f, 0.0f, 0.0f) & 0xFFu;
+  if (data) {
+    const float sc = __fmul_rn(e4m3_value(code), g);
+    uint32_t packed = 0;
+    if (sc != 0.0f) {
+      const GroupDiv div(sc);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) packed |= cvt2_e2m1(div(v[2 * j]), div(v[2 * j + 1])) << (8 * j);
+    }
+    *reinterpret_cast<uint32_t*>(q + row * (cols / 2) + col / 2) = packed;
+  }
+  if ((lane & 1) == 0 && b < kb_pad) {
+    const uint8_t c = data ? static_cast<uint8_t>(code) : static_cast<uint8_t>(0);
+    if (kTC) {
+      sf[sf_tc_offset(row, b, kb_pad / 4)] = c;
+    } else if (data) {
+      sf[row * kb + b] = c;
+    }
+  }
+}
+
 __global__ void sf_to_tcgen05_kernel(const uint8_t* __restrict__ sf, int64_t rows, int64_t kb,
                                      int64_t total, uint8_t* __restrict__ out) {
   grid_dep_launch();
@@ -326,6 +383,23 @@ cudaError_t launch_quantize_mx(const void* x, bool src_bf16, int64_t rows, int64
   if (fmt < 0 || fmt > 2) return cudaErrorInvalidValue;
   const K kern = table[fmt][src_bf16 ? 1 : 0][tc_layout ? 1 : 0];
   return launch_pdl(kern, dim3(blocks), dim3(256), 0, s, x, rows, cols, ld, fmt_max, vec_in, q, sf);
+}
+
+cudaError_t launch_quantize_nvfp4(const void* x, bool src_bf16, int64_t rows, int64_t cols,
+                                  int64_t ld, float tensor_scale, uint8_t* q, uint8_t* sf,
+                                  bool tc_layout, cudaStream_t s) {
+  const bool vec_in = src_bf16 ? (aligned(x, 8) && ld % 4 == 0) : (aligned(x, 16) && ld % 4 == 0);
+  const int64_t kb = cols / 16;
+  const int64_t kb_pad = tc_layout ? ((kb + 3) / 4) * 4 : kb;
+  const int64_t rows_pad = tc_layout ? ((rows + 127) / 128) * 128 : rows;
+  const int64_t warps = rows_pad * ((kb_pad + 15) / 16);
+  const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
+  using K = void (*)(const void*, int64_t, int64_t, int64_t, float, bool, uint8_t*, uint8_t*);
+  static const K table[2][2] = {{quantize_nvfp4_kernel<false, false>, quantize_nvfp4_kernel<false, true>},
+                                {quantize_nvfp4_kernel<true, false>, quantize_nvfp4_kernel<true, true>}};
+  const K kern = table[src_bf16 ? 1 : 0][tc_layout ? 1 : 0];
+  return launch_pdl(kern, dim3(blocks), dim3(256), 0, s, x, rows, cols, ld, tensor_scale, vec_in, q,
+                    sf);
 }
 
 cudaError_t launch_sf_to_tcgen05(const uint8_t* sf, int64_t rows, int64_t kblocks, uint8_t* out,

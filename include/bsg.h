@@ -75,7 +75,10 @@ typedef enum {
      [ceil(C/128)][R], so the scales of one K tile are contiguous.            */
   BSG_SCALE_ROW1x128 = 1,
   /* One E8M0 scale per 1 x 32 block along K (MXFP4); layout per bsg_sf_layout */
-  BSG_SCALE_BLOCK1x32_E8M0 = 2
+  BSG_SCALE_BLOCK1x32_E8M0 = 2,
+  /* One E4M3 scale per 1 x 16 block along K (NVFP4); layout per bsg_sf_layout,
+     tcgen05 padding bytes 0.                                                  */
+  BSG_SCALE_BLOCK1x16_E4M3 = 3
 } bsg_scale_gran;
 
 typedef enum {
@@ -157,6 +160,32 @@ bsg_status bsg_quantize_mx(const void* x, bsg_dtype src, int64_t rows, int64_t c
                            bsg_format fmt, float fmt_max, uint8_t* q, uint8_t* sf,
                            bsg_sf_layout layout, void* stream);
 
+/* bsg_quantize_nvfp4 - NVFP4 quantisation: E2M1 elements, one E4M3 scale per
+ * 16 elements along K, one FP32 tensor scale g.
+ *
+ * "Rubin FP4 GEMM deep dive", section 5.3 (blocks of 16 give finer scales) and
+ * section 2.2 (the block scale kept in a higher-precision format such as FP8).
+ * Per block: v = max|x| / 6 and u = v / g (FP32, round to nearest); the scale
+ * code is u rounded to E4M3 (nearest even, saturating at 448); the block's
+ * scale is s = E4M3(code) * g (FP32); each element is x / s (IEEE FP32
+ * division) rounded to E2M1 (nearest even, saturating at 6); a block whose s
+ * is 0 stores zero codes.  g (not on the pages) lets the E4M3 scales cover
+ * data of any magnitude; pass alpha = g_A * g_B to bsg_gemm_nvfp4.
+ *
+ * x, src, rows, ld  as bsg_quantize_mxfp4.
+ * cols     K extent, a multiple of 16.
+ * tensor_scale  g: finite, >= 2^-126.
+ * q_packed device, rows x cols/2 bytes (first element in the low nibble),
+ *          4-byte aligned.
+ * sf       device, E4M3 codes in `layout` (bsg_scale_bytes with
+ *          BSG_SCALE_BLOCK1x16_E4M3 gives the size; tcgen05 padding 0).
+ * Errors: BSG_ERR_INVALID_ARG (null, sizes, cols % 16, bad g),
+ *         BSG_ERR_ALIGNMENT, BSG_ERR_CUDA.
+ */
+bsg_status bsg_quantize_nvfp4(const void* x, bsg_dtype src, int64_t rows, int64_t cols,
+                              int64_t ld, float tensor_scale, uint8_t* q_packed, uint8_t* sf,
+                              bsg_sf_layout layout, void* stream);
+
 /* bsg_gemm - block-scaled GEMM D = sum_k (s_A a_k)(s_B b_k) + C.
  *
  * "FP8 GEMM on CDNA4", sections 2.2 (FP32 accumulation), 3.3 and 4.4 (the
@@ -177,7 +206,9 @@ bsg_status bsg_quantize_mx(const void* x, bsg_dtype src, int64_t rows, int64_t c
  *         128-wide K tile), or - for both operands together - MXFP8:
  *         BSG_SCALE_BLOCK1x32_E8M0 in the BSG_SF_TCGEN05 layout (applied by
  *         the tensor core, as bsg_quantize_mx writes them); E2M1 ->
- *         BSG_SCALE_BLOCK1x32_E8M0 in the BSG_SF_TCGEN05 layout.
+ *         BSG_SCALE_BLOCK1x32_E8M0 in the BSG_SF_TCGEN05 layout (MXFP4), or
+ *         BSG_SCALE_BLOCK1x16_E4M3 in that layout for both operands (NVFP4,
+ *         alpha 1; see bsg_gemm_nvfp4).
  * sB, gb  B's scales, same rules with N in place of M.
  * C   device, optional (NULL) FP32 M x N row-major addend.
  * D   device, M x N row-major output, FP32 or BF16 (round to nearest even).
@@ -228,6 +259,22 @@ bsg_status bsg_gemm_quantized(int64_t M, int64_t N, int64_t K,
                               const void* B, bsg_format fb, const void* sB, bsg_scale_gran gb,
                               const float* C, bsg_format qfmt, float fmt_max,
                               uint8_t* Dq, float* sD, void* stream);
+
+/* bsg_gemm_nvfp4 - NVFP4 GEMM D = alpha * sum_k (s_A a_k)(s_B b_k) + C.
+ *
+ * A, B: packed E2M1 (M x K/2 and N x K/2 bytes, B = K x N column-major);
+ * sA, sB: E4M3 block scales in the BSG_SF_TCGEN05 layout as
+ * bsg_quantize_nvfp4 writes them; the tensor core applies them (kind::
+ * mxf4nvf4, FP32 accumulation across all of K).  alpha (finite; normally
+ * g_A * g_B) multiplies the FP32 sum before the addend C (optional FP32
+ * M x N).  D: FP32 or BF16 (nearest even), M x N row-major.  bsg_gemm with
+ * BSG_SCALE_BLOCK1x16_E4M3 on both operands is the same with alpha = 1.
+ * Constraints: K % 32 == 0; A, B, sA, sB 16-byte aligned.
+ * Errors: BSG_ERR_INVALID_ARG, BSG_ERR_ALIGNMENT, BSG_ERR_CUDA.
+ */
+bsg_status bsg_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const void* A, const void* sA,
+                          const void* B, const void* sB, float alpha, const float* C, void* D,
+                          bsg_dtype out, void* stream);
 
 /* Bytes of device workspace bsg_gemm needs for this problem (0 if none). */
 size_t bsg_gemm_workspace_size(int64_t M, int64_t N, int64_t K, bsg_format fa, bsg_format fb);

@@ -1,0 +1,90 @@
+"""NVFP4 (E2M1 elements, E4M3 scales per 16 along K, FP32 tensor scale):
+quantiser bit-exact against the oracle, GEMM within the stated tolerance
+|D - D_ref| <= 1e-4 * sum_k |s_A a_k s_B b_k| + 1e-6 (BF16: + 8e-3 |D_ref|)."""
+import numpy as np
+import pytest
+
+import synth
+from helpers import device, report, to_dev
+from oracle import gemm as og
+from oracle import quantize as oq
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16_tensor(x, dev):
+    import torch
+    bits = synth.to_bf16_bits(x)
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 16), (7, 48), (200, 272), (130, 1024)])
+@pytest.mark.parametrize("g", [1.0, 2.0 ** -7, 0.0123])
+@pytest.mark.parametrize("src", ["f32", "bf16"])
+def test_quantize_nvfp4_bit_exact(rows, cols, g, src):
+    import fp4_gemm_gb300 as bsg
+    dev = device()
+    rng = np.random.default_rng(rows * 1000 + cols)
+    x = (rng.standard_normal((rows, cols)) * np.exp2(rng.uniform(-10, 6, (rows, 1)))).astype(np.float32)
+    x[0, :16] = 0.0                                         # a zero block
+    if cols >= 48:
+        x[-1, 16:32] *= np.float32(1e-6)                     # a block whose scale underflows
+        x[-1, 32:48] = np.float32(6000.0)                    # a block whose scale saturates
+    xt = _bf16_tensor(x, dev) if src == "bf16" else to_dev(x, dev)
+    xr = synth.bf16_bits_to_f32(synth.to_bf16_bits(x)) if src == "bf16" else x
+    op, osf = oq.quantize_nvfp4(xr, tensor_scale=g)
+    p, sf = bsg.bsg_quantize_nvfp4(xt, "rowmajor", tensor_scale=g)
+    assert bsg.bsg_device_error() == 0
+    assert np.array_equal(p.cpu().numpy(), op)
+    assert np.array_equal(sf.cpu().numpy(), osf)
+    p2, sf2 = bsg.bsg_quantize_nvfp4(xt, "tcgen05", tensor_scale=g)
+    assert np.array_equal(p2.cpu().numpy(), op)
+    assert np.array_equal(sf2.cpu().numpy(), oq.sf_to_tcgen05_layout(osf, pad=0))
+
+
+def _gemm(M, N, K, ga=1.0, gb=2.0 ** -6, out="f32", addend=False, via_bsg_gemm=False, rows=None,
+          cols=None, workload="ffn_up"):
+    import fp4_gemm_gb300 as bsg
+    dev = device()
+    A, B = synth.make(workload, m=M, n=N, k=K)
+    qa, sa = bsg.bsg_quantize_nvfp4(to_dev(A, dev), tensor_scale=ga)
+    qb, sb = bsg.bsg_quantize_nvfp4(to_dev(B, dev), tensor_scale=gb)
+    C = synth.addend(workload, M, N) if addend else None
+    Ct = None if C is None else to_dev(C, dev)
+    alpha = float(np.float32(ga) * np.float32(gb))
+    if via_bsg_gemm:
+        assert alpha == 1.0
+        D = bsg.bsg_gemm(qa, "e2m1", sa, "nv", qb, "e2m1", sb, "nv", C=Ct, out=out)
+    else:
+        D = bsg.bsg_gemm_nvfp4(qa, sa, qb, sb, alpha=alpha, C=Ct, out=out)
+    assert bsg.bsg_device_error() == 0
+    D = D.float().cpu().numpy()
+    ri = np.arange(M) if rows is None else np.asarray(rows)
+    ci = np.arange(N) if cols is None else np.asarray(cols)
+    pa, fa = oq.quantize_nvfp4(A[ri], tensor_scale=ga)      # scales are per row: rows quantise alone
+    pb, fb = oq.quantize_nvfp4(B[ci], tensor_scale=gb)
+    Csub = None if C is None else C[np.ix_(ri, ci)]
+    Dref, bnd = og.gemm_nvfp4(pa, fa, pb, fb, alpha=alpha, C=Csub)
+    return og.within_tolerance(D[np.ix_(ri, ci)], Dref, bnd, bf16=out == "bf16")
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 300, 288), (1, 256, 128), (129, 257, 96), (384, 520, 1056)])
+@pytest.mark.parametrize("out,addend", [("f32", False), ("bf16", True)])
+def test_nvfp4_gemm_ragged(M, N, K, out, addend):
+    report(f"nvfp4 {M}x{N}x{K} {out}", *_gemm(M, N, K, out=out, addend=addend))
+
+
+def test_nvfp4_gemm_through_bsg_gemm():
+    report("nvfp4 via bsg_gemm", *_gemm(256, 384, 512, ga=1.0, gb=1.0, via_bsg_gemm=True))
+
+
+def test_nvfp4_gemm_1024_cube_wide_rows():
+    report("nvfp4 1024^3", *_gemm(1024, 1024, 1024, ga=2.0 ** -2, gb=2.0 ** -2, workload="mxfp4_1024"))
+
+
+def test_nvfp4_gemm_ffn_up_full_size_sampled():
+    _, M, N, K = synth.WORKLOADS["ffn_up"]
+    g = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([[0, 127, 128, M - 1], g.integers(0, M, 28)]))
+    cols = np.unique(np.concatenate([[0, 127, 128, N - 1], g.integers(0, N, 60)]))
+    report("nvfp4 ffn_up sampled", *_gemm(M, N, K, ga=1.0, gb=2.0 ** -6, out="bf16", rows=rows, cols=cols))
