@@ -18,6 +18,10 @@ Workloads (synthetic, seeded; see synth/):
               E8M0 scale per 32 along K, applied by the tensor core, so the
               GEMM needs no promotion): quantise the activations with the MX
               rule, then the block-scaled FP8 GEMM, BF16 out.
+  nvfp4_ffn_up  the FFN-up shape with NVFP4 operands (E2M1, one E4M3 scale per
+              16 along K, FP32 tensor scales: 1 for the activations, 2^-6
+              for the weights): quantise the activations, then the block-
+              scaled FP4 GEMM (alpha = 2^-6), BF16 out.
   ffn_up_q8out  the FFN-up step with the quantiser fused into the GEMM's
               epilogue: the output leaves as E4M3 codes with one FP32 scale
               per 1x128 run of a row (the next GEMM's activation operand)
@@ -68,7 +72,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {"fp8": ["gemm_fp8.cu", "common.cuh", "quant_math.cuh"], "fp4": ["gemm_mxfp4.cu", "common.cuh"],
                   "mx8": ["gemm_mx.cu", "common.cuh"]}
 # workloads that reuse another workload's shape and seeded inputs
-SHAPE_OF = {"mxfp8_ffn_up": "ffn_up", "ffn_up_q8out": "ffn_up"}
+SHAPE_OF = {"mxfp8_ffn_up": "ffn_up", "ffn_up_q8out": "ffn_up", "nvfp4_ffn_up": "ffn_up"}
 
 
 def kernel_source_hash(files):
@@ -109,7 +113,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="ffn_up",
                     choices=["ffn_up", "dgrad", "decode", "fp8_256", "mxfp4_1024", "mxfp8_ffn_up",
-                             "ffn_up_q8out"])
+                             "ffn_up_q8out", "nvfp4_ffn_up"])
     ap.add_argument("--m", type=int, default=None, help="override M (e.g. 1 for decode)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -134,10 +138,14 @@ class Workload:
         self.fp4 = name in ("decode", "mxfp4_1024")
         self.mx8 = name == "mxfp8_ffn_up"
         self.q8out = name == "ffn_up_q8out"
+        self.nv4 = name == "nvfp4_ffn_up"
+        self.g_a, self.g_b = 1.0, 2.0 ** -6      # NVFP4 tensor scales
         if name == "ffn_up":
             self.fa, self.fb, self.ga, self.gb, self.out = "e4m3", "e4m3", "row", "tile", "bf16"
         elif self.q8out:
             self.fa, self.fb, self.ga, self.gb, self.out = "e4m3", "e4m3", "row", "tile", "e4m3/row"
+        elif self.nv4:
+            self.fa, self.fb, self.ga, self.gb, self.out = "e2m1", "e2m1", "nv", "nv", "bf16"
         elif name == "dgrad":
             self.fa, self.fb, self.ga, self.gb, self.out = "e5m2", "e4m3", "tile", "tile", "f32"
         elif name == "fp8_256":
@@ -157,7 +165,9 @@ class Workload:
         A0 = self.A_host_t.to(dev)
         Bt = torch.from_numpy(B).to(dev)
         # weights are quantised once, outside the step (static parameters)
-        if self.fp4:
+        if self.nv4:
+            qb, sb = bsg.bsg_quantize_nvfp4(Bt, "tcgen05", tensor_scale=self.g_b)
+        elif self.fp4:
             qb, sb = bsg.bsg_quantize_mxfp4(Bt, "tcgen05")
         elif self.mx8:
             qb, sb = bsg.bsg_quantize_mx(Bt, self.fb, "tcgen05")
@@ -174,7 +184,9 @@ class Workload:
         for r in range(self.nsets):
             st = {"A": A0 if r == 0 else A0.clone(),
                   "qb": qb if r == 0 else qb.clone(), "sb": sb if r == 0 else sb.clone()}
-            if self.fp4:
+            if self.nv4:
+                st["qa"], st["sa"] = bsg.bsg_quantize_nvfp4(st["A"], "tcgen05", tensor_scale=self.g_a)
+            elif self.fp4:
                 st["qa"], st["sa"] = bsg.bsg_quantize_mxfp4(st["A"], "tcgen05")
             elif self.mx8:
                 st["qa"], st["sa"] = bsg.bsg_quantize_mx(st["A"], self.fa, "tcgen05")
@@ -195,7 +207,9 @@ class Workload:
 
     def quantize(self, r=0):
         b, st = self.bsg, self.sets[r]
-        if self.fp4:
+        if self.nv4:
+            b.bsg_quantize_nvfp4(st["A"], "tcgen05", tensor_scale=self.g_a, q=st["qa"], sf=st["sa"])
+        elif self.fp4:
             b.bsg_quantize_mxfp4(st["A"], "tcgen05", q=st["qa"], sf=st["sa"])
         elif self.mx8:
             b.bsg_quantize_mx(st["A"], self.fa, "tcgen05", q=st["qa"], sf=st["sa"])
@@ -204,6 +218,10 @@ class Workload:
 
     def gemm(self, r=0):
         st = self.sets[r]
+        if self.nv4:
+            self.bsg.bsg_gemm_nvfp4(st["qa"], st["sa"], st["qb"], st["sb"], alpha=self.g_a * self.g_b,
+                                    out=self.out, D=st["D"], K=self.K)
+            return
         if self.q8out:
             self.bsg.bsg_gemm_quantized(st["qa"], self.fa, st["sa"], self.ga, st["qb"], self.fb, st["sb"],
                                         self.gb, qfmt="e4m3", Dq=st["D"], sD=st["sD"])
@@ -224,7 +242,10 @@ class Workload:
     def gemm_bytes(self):
         """Bytes a GEMM must move at least once: operands, scales, output."""
         M, N, K = self.M, self.N, self.K
-        if self.fp4:
+        if self.nv4:
+            a = M * K / 2 + M * K / 16
+            b = N * K / 2 + N * K / 16
+        elif self.fp4:
             a = M * K / 2 + M * K / 32
             b = N * K / 2 + N * K / 32
         elif self.mx8:
@@ -347,6 +368,18 @@ def cpu_baseline(name, m_override, target_s=15.0):
                 "kind": "oracle",
                 "sample": f"{name}: {rows} of {M} rows of A with {ncols} of {N} rows of B (K={K}); "
                           f"oracle MXFP8 quantise (both operands) + FP64 GEMM, {dt:.1f} s"}
+    if name == "nvfp4_ffn_up":
+        rows, ncols = 128, 2048
+        A, B = synth.make("ffn_up", m=rows, n=ncols)
+        t0 = time.perf_counter()
+        pa, fa = oq.quantize_nvfp4(A)
+        pb, fb = oq.quantize_nvfp4(B, tensor_scale=2.0 ** -6)
+        og.gemm_nvfp4(pa, fa, pb, fb, alpha=2.0 ** -6)
+        dt = time.perf_counter() - t0
+        return {"value": 2.0 * rows * ncols * K / dt / 1e12, "unit": "TFLOP/s", "cores": cores,
+                "kind": "oracle",
+                "sample": f"{name}: {rows} of {M} rows of A with {ncols} of {N} rows of B (K={K}); "
+                          f"oracle NVFP4 quantise (both operands) + FP64 GEMM, {dt:.1f} s"}
     if name == "ffn_up_q8out":
         rows = 128
         A, B = synth.make("ffn_up", m=rows)
@@ -577,11 +610,11 @@ def main():
                 "kernel": "gemm_mxfp4_decode_kernel",
                 "peak_source": f"{pk_kind} HBM copy bandwidth"}
     else:
-        dt = "fp4" if w.fp4 else "fp8"
+        dt = "fp4" if (w.fp4 or w.nv4) else "fp8"
         achieved = w.flops() / g_s / 1e12
         peak = pk["bf16_tflops"] * RATIO[dt]
         src_kind = "mx8" if w.mx8 else dt
-        kernel = "gemm_mxfp4_kernel" if w.fp4 else ("gemm_mx_kernel" if w.mx8 else "gemm_fp8_kernel")
+        kernel = "gemm_mxfp4_kernel" if (w.fp4 or w.nv4) else ("gemm_mx_kernel" if w.mx8 else "gemm_fp8_kernel")
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": measured_traffic(w.name, src_kind),
                 "kernel": kernel,
@@ -591,7 +624,9 @@ def main():
         # the tensor core's own rate for this kind, measured now on this GPU
         # (outside the timed region): context beside the official peak
         from fp4_gemm_gb300 import peak as mma_peak
-        kind = ("e2m1", True) if w.fp4 else (("e4m3", True) if w.mx8 else ("e4m3", False))
+        # (NVFP4 is timed against the MXFP4 microbenchmark: the peak tool has
+        # no scale_vec::4X kind)
+        kind = ("e2m1", True) if (w.fp4 or w.nv4) else (("e4m3", True) if w.mx8 else ("e4m3", False))
         mp, _ = mma_peak.measure(kind[0], kind[1], False, 1 << 14, 5)
         roof["mma_peak_microbench"] = mp
         roof["frac_of_mma_peak_microbench"] = roof["achieved"] / mp
@@ -600,7 +635,7 @@ def main():
     line = {
         "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e2m1" if w.fp4 else (w.fa if w.fa == w.fb else f"{w.fa}x{w.fb}"),
+        "vs_baseline": None, "dtype": "e2m1" if (w.fp4 or w.nv4) else (w.fa if w.fa == w.fb else f"{w.fa}x{w.fb}"),
         "data": "synthetic (seeded; weights random-init and pre-quantised)",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
                    "a": f"{w.fa}/{w.ga}", "b": f"{w.fb}/{w.gb}", "out": w.out,
