@@ -417,6 +417,17 @@ def cpu_baseline(name, m_override, target_s=15.0):
 
 
 # -------------------------------------------------------------------- runs
+def max_over_ranks(value, dist, device):
+    """The largest of every rank's value (the job's time is its slowest
+    rank's); `value` itself on a single process."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -560,10 +571,7 @@ def main():
     if bsg.bsg_device_error() != 0:
         raise RuntimeError("device error during the timed steps")
     ms = step_ms_mean
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
 
     # end to end through the API with host buffers (rotating over the same
     # input sets as the device-timed steps)
@@ -592,10 +600,7 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1) / K
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_ms, dist, dev)
         e2e = {"value": world * w.value_from_seconds(e_ms / 1e3), "unit": w.metric()[1],
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e_ms}
