@@ -145,6 +145,29 @@ bsg_status run_fp8(Fp8GemmArgs* a, const void* A, const void* B, int out_elem_by
   return from_cuda(bsg::launch_gemm_fp8(*a, sms, s));
 }
 
+// The 128 x 256 block-scaled kernel for large FP4 problems (kind 1 MXFP4,
+// 2 NVFP4); operands packed, K/2 bytes per row.
+bsg_status run_fp4_large(int kind, float alpha, int64_t M, int64_t N, int64_t K, const void* A,
+                         const void* sA, const void* B, const void* sB, const float* C, void* D,
+                         bool out_bf16, int sms, cudaStream_t s) {
+  bsg::MxGemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.kind = kind;
+  a.alpha = alpha;
+  a.sfA = static_cast<const uint8_t*>(sA);
+  a.sfB = static_cast<const uint8_t*>(sB);
+  a.C = C;
+  a.D = D;
+  a.out_bf16 = out_bf16;
+  if (!make_kmajor_map(&a.tmA, A, K / 2, M, K / 2, 128) ||
+      !make_kmajor_map(&a.tmB, B, K / 2, N, K / 2, static_cast<uint32_t>(bsg::gemm_mx_b_box_rows())))
+    return BSG_ERR_CUDA;
+  return from_cuda(bsg::launch_gemm_mx(a, sms, s));
+}
+
 }  // namespace
 
 extern "C" {
@@ -366,9 +389,12 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
     a.workspace_bytes = workspace_bytes;
     a.A = A;
     a.B = B;
-    if (ga == BSG_SCALE_BLOCK1x16_E4M3) {
-      // NVFP4: the general kernel at every M, tensor scales folded into alpha
-      // by bsg_gemm_nvfp4 (1 here)
+    const bool nv = ga == BSG_SCALE_BLOCK1x16_E4M3;
+    if ((nv || M > kDecodeMaxM) && bsg::gemm_mx_fp4_large(a.M, a.N, sms))
+      return run_fp4_large(nv ? 2 : 1, 1.0f, M, N, K, A, sA, B, sB, C, D, out == BSG_BF16, sms, s);
+    if (nv) {
+      // NVFP4 below the large-kernel size: the general kernel (no decode
+      // path); tensor scales are folded into alpha by bsg_gemm_nvfp4 (1 here)
       a.nvfp4 = true;
       a.alpha = 1.0f;
     } else if (M <= kDecodeMaxM) {
@@ -402,6 +428,8 @@ bsg_status bsg_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const void* A, const 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int sms = num_sms_current();
   if (sms <= 0) return BSG_ERR_CUDA;
+  if (bsg::gemm_mx_fp4_large(static_cast<int>(M), static_cast<int>(N), sms))
+    return run_fp4_large(2, alpha, M, N, K, A, sA, B, sB, C, D, out == BSG_BF16, sms, s);
   Mxfp4GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.M = static_cast<int>(M);

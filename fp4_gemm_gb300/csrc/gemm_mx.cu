@@ -1,6 +1,18 @@
-// Block-scaled MXFP8 GEMM for large shapes, for sm_103a.
+// Block-scaled GEMMs for large shapes, for sm_103a: MXFP8, MXFP4, NVFP4.
 //
-//   D[i][j] = sum_k (2^eA(i,k/32) a[i][k]) (2^eB(j,k/32) b[j][k]) + C[i][j]
+//   D[i][j] = alpha * sum_k (sA(i,k) a[i][k]) (sB(j,k) b[j][k]) + C[i][j]
+//
+// Three operand kinds share this kernel (kKind):
+//   MXFP8  FP8 E4M3/E5M2, UE8M0 per 32 along K, kind::mxf8f6f4 scale_vec::1X
+//          (K = 32 per MMA, one scale byte per row); a stage is 128 K.
+//   MXFP4  packed E2M1, UE8M0 per 32, kind::mxf4 scale_vec::2X (K = 64 per
+//          MMA, two scale bytes); a stage is 256 K = 2 scale atoms per 128
+//          rows.
+//   NVFP4  packed E2M1, UE4M3 per 16, kind::mxf4nvf4 scale_vec::4X (K = 64,
+//          four scale bytes = one atom per MMA); a stage is 256 K = 4 atoms;
+//          the sum is multiplied by alpha (the product of the tensor scales).
+// In every kind a stage is 128 bytes of each operand row, so the MMA time and
+// the bytes moved per stage are the same; the text below describes MXFP8.
 //
 // The K-blocked scaling of "Rubin FP4 GEMM deep dive" (sections 2.2 and 3.1:
 // 32 consecutive K elements share one E8M0 scale, each block's partial sum
@@ -47,8 +59,7 @@ __device__ uint32_t g_mx_error = 0;
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int kRowBytes = 128;          // bytes of an operand row per stage = 128 FP8 values
-constexpr int kStages = 4;
+constexpr int kRowBytes = 128;          // bytes of an operand row per stage (128 FP8 / 256 FP4 values)
 constexpr int kThreads = 512;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
@@ -61,19 +72,38 @@ static_assert(128 * kRegsSmall * 2 + 256 * kRegsLarge <= kThreads * 128,
 constexpr int kSfAtom = 512;            // 128 rows x 4 K-blocks of E8M0
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = BN;            // FP32 accumulator columns
-constexpr int kSfColsPerStage = 16;     // SFA atom: 4 columns (+4 free), SFB atoms: 2 x 4 columns
 constexpr int kGroup = 8;
-static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "tensor memory columns");
 
+enum Kind : int { kMxfp8 = 0, kMxfp4 = 1, kNvfp4 = 2 };
+
+// Per kind: scale atoms (512 bytes = 128 rows x 4 scale bytes) per 128 rows
+// per stage, the scale block along K, and the tensor-memory columns of a
+// stage's scales: A's atoms (4 columns each) from the stage's first column,
+// B's from sfb_off; B's K-atom j puts its two 128-row blocks at sfb_off + 8j
+// and + 4 (the 256 rows of one N = 256 MMA, 8-column aligned).
+template <int kKind>
+struct KindCfg {
+  static constexpr int kAtoms = kKind == kMxfp8 ? 1 : (kKind == kMxfp4 ? 2 : 4);
+  static constexpr int kBlock = kKind == kNvfp4 ? 16 : 32;
+  static constexpr int kSfbOff = kAtoms * 4 > 8 ? kAtoms * 4 : 8;
+  static constexpr int kSfColsPerStage = kSfbOff + 8 * kAtoms;
+  // NVFP4's 6 KB of scales per stage leave room for three stages
+  static constexpr int kStages = kKind == kNvfp4 ? 3 : 4;
+  static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "tensor memory columns");
+};
+
+template <int kKind>
 struct __align__(1024) Smem {
-  uint8_t a[kStages][BM * kRowBytes];
-  uint8_t b[kStages][BN * kRowBytes];
+  static constexpr int S = KindCfg<kKind>::kStages;
+  static constexpr int A = KindCfg<kKind>::kAtoms;
+  uint8_t a[S][BM * kRowBytes];
+  uint8_t b[S][BN * kRowBytes];
   uint8_t epi[8][32 * 64];     // per epilogue warp: 32 rows x 64 B output staging
-  uint8_t sfa[kStages][kSfAtom];
-  uint8_t sfb[kStages][2 * kSfAtom];
-  uint64_t full[kStages];
-  uint64_t sready[kStages];   // the stage's scales are in tensor memory
-  uint64_t done[kStages];
+  uint8_t sfa[S][A * kSfAtom];
+  uint8_t sfb[S][2][A * kSfAtom];   // B's two 128-row blocks
+  uint64_t full[S];
+  uint64_t sready[S];         // the stage's scales are in tensor memory
+  uint64_t done[S];
   uint64_t tfull;
   uint64_t tempty;
   uint64_t final_bar;
@@ -104,21 +134,27 @@ __device__ __forceinline__ void raise_abort(volatile uint32_t* flag) {
   *flag = 1u;
 }
 
-template <bool kBF16Out>
+template <bool kBF16Out, int kKind>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const uint8_t* __restrict__ sfA, const uint8_t* __restrict__ sfB,
                    const float* __restrict__ Cin, void* __restrict__ Dout, int M, int N, int K,
-                   uint32_t afmt, uint32_t bfmt, bool vec_out, bool raster_n) {
+                   uint32_t afmt, uint32_t bfmt, bool vec_out, bool raster_n, float alpha) {
+  using KC = KindCfg<kKind>;
+  constexpr int kStages = KC::kStages;
+  constexpr int kAtoms = KC::kAtoms;
+  constexpr int kSfColsPerStage = KC::kSfColsPerStage;
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                      ~static_cast<uintptr_t>(1023));
+  Smem<kKind>& sm = *reinterpret_cast<Smem<kKind>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
   const int num_m = (M + BM - 1) / BM;
   const int num_n = (N + BN - 1) / BN;
   const int tiles = num_m * num_n;
-  const int KS = (K + kRowBytes - 1) / kRowBytes;   // stages along K = scale atoms along K
+  const int kbytes = kKind == kMxfp8 ? K : K / 2;  // operand bytes per row
+  const int KS = (kbytes + kRowBytes - 1) / kRowBytes;   // stages along K
+  const int KA = (K / KC::kBlock + 3) / 4;          // scale atoms along K
   const int num_nb = (N + 127) / 128;               // 128-row blocks of B
 
   if (threadIdx.x == 0) {
@@ -168,14 +204,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t fb = smem_u32(&sm.full[s]);
-          mbar_arrive_expect_tx(fb, (BM + BN) * kRowBytes + (1 + nbv) * kSfAtom);
+          const int ka0 = ks * kAtoms;
+          const int na = min(kAtoms, KA - ka0);               // atoms of this stage
+          mbar_arrive_expect_tx(fb, (BM + BN) * kRowBytes + (1 + nbv) * na * kSfAtom);
           tma_load_2d_hint(smem_u32(sm.a[s]), &tmA, fb, ks * kRowBytes, tc.m * BM, keep);
           tma_load_2d_hint(smem_u32(sm.b[s]), &tmB, fb, ks * kRowBytes, tc.n * BN, keep);
-          bulk_load(smem_u32(sm.sfa[s]), sfA + (static_cast<int64_t>(tc.m) * KS + ks) * kSfAtom,
-                    kSfAtom, fb);
+          // a row block's atoms along K are contiguous: one copy per block
+          bulk_load(smem_u32(sm.sfa[s]), sfA + (static_cast<int64_t>(tc.m) * KA + ka0) * kSfAtom,
+                    na * kSfAtom, fb);
           for (int j = 0; j < nbv; ++j)
-            bulk_load(smem_u32(sm.sfb[s] + j * kSfAtom),
-                      sfB + (static_cast<int64_t>(2 * tc.n + j) * KS + ks) * kSfAtom, kSfAtom, fb);
+            bulk_load(smem_u32(sm.sfb[s][j]),
+                      sfB + (static_cast<int64_t>(2 * tc.n + j) * KA + ka0) * kSfAtom, na * kSfAtom, fb);
         }
       }
       drain_fills(sm.full, kStages, it);
@@ -211,19 +250,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ks = 0; ks < KS && ok; ++ks, ++it) {
           const int s = static_cast<int>(it % kStages);
           const uint32_t sfa_t = tmem + kAccCols + s * kSfColsPerStage;
-          const uint32_t sfb_t = sfa_t + 8;
+          const uint32_t sfb_t = sfa_t + KC::kSfbOff;
           const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sm.a[s]));
           const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sm.b[s]));
-          const int rem = K - ks * kRowBytes;
+          const int rem = kbytes - ks * kRowBytes;           // 32 bytes per MMA
           const int nk = rem >= kRowBytes ? 4 : (rem + 31) / 32;
           const bool more = ks + 1 < KS;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             if (kk < nk) {
-              // K block kk of the atom: scale byte kk of each row's column
-              mma_mxf8(tmem, ad + 2 * kk, bd + 2 * kk,
-                       idesc_mxf8(afmt, bfmt, BM, BN, static_cast<uint32_t>(kk), static_cast<uint32_t>(kk)),
-                       sfa_t, sfb_t, (ks > 0 || kk > 0) ? 1u : 0u);
+              const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
+              if (kKind == kMxfp8) {
+                // K block kk of the atom: scale byte kk of each row's cell
+                mma_mxf8(tmem, ad + 2 * kk, bd + 2 * kk,
+                         idesc_mxf8(afmt, bfmt, BM, BN, static_cast<uint32_t>(kk), static_cast<uint32_t>(kk)),
+                         sfa_t, sfb_t, acc);
+              } else if (kKind == kMxfp4) {
+                // K = 64: half of atom kk / 2, bytes 0-1 or 2-3 of each cell
+                const uint32_t id = static_cast<uint32_t>((kk & 1) * 2);
+                mma_mxf4(tmem, ad + 2 * kk, bd + 2 * kk, idesc_mxf4(BM, BN, id, id),
+                         sfa_t + 4 * (kk >> 1), sfb_t + 8 * (kk >> 1), acc);
+              } else {
+                // K = 64: all four bytes of atom kk
+                mma_nvf4(tmem, ad + 2 * kk, bd + 2 * kk, idesc_nvf4(BM, BN), sfa_t + 4 * kk,
+                         sfb_t + 8 * kk, acc);
+              }
             }
             if (kk == 1 && more &&
                 !mbar_wait(smem_u32(&sm.sready[(it + 1) % kStages]), ((it + 1) / kStages) & 1u)) {
@@ -262,10 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint32_t sfa_t = tmem + lane_off + kAccCols + s * kSfColsPerStage;
-        const uint32_t sfb_t = sfa_t + 8;
-        tmem_st_4(sfa_t, ld_shared_v4(smem_u32(sm.sfa[s]) + lane * 16));
-        tmem_st_4(sfb_t, ld_shared_v4(smem_u32(sm.sfb[s]) + lane * 16));
-        tmem_st_4(sfb_t + 4, ld_shared_v4(smem_u32(sm.sfb[s]) + kSfAtom + lane * 16));
+        const uint32_t sfb_t = sfa_t + KC::kSfbOff;
+        const int na = min(kAtoms, KA - ks * kAtoms);
+#pragma unroll
+        for (int a = 0; a < kAtoms; ++a) {
+          if (a < na) {
+            tmem_st_4(sfa_t + 4 * a, ld_shared_v4(smem_u32(sm.sfa[s]) + a * kSfAtom + lane * 16));
+            tmem_st_4(sfb_t + 8 * a, ld_shared_v4(smem_u32(sm.sfb[s][0]) + a * kSfAtom + lane * 16));
+            tmem_st_4(sfb_t + 8 * a + 4, ld_shared_v4(smem_u32(sm.sfb[s][1]) + a * kSfAtom + lane * 16));
+          }
+        }
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -319,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < kPerPiece; ++j) {
             const int col = ch * kColsPerChunk + p * kPerPiece + j;
             v[j] = __uint_as_float(r[col / 32][col % 32]);
+            if (kKind == kNvfp4) v[j] *= alpha;
           }
           if (Cin != nullptr && my_row < M) {
 #pragma unroll
@@ -379,10 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool kBF16Out>
+template <bool kBF16Out, int kKind>
 cudaError_t launch_variant(const MxGemmArgs& a, int num_sms, cudaStream_t s) {
-  auto kern = gemm_mx_kernel<kBF16Out>;
-  const size_t smem = sizeof(Smem) + 1024;
+  auto kern = gemm_mx_kernel<kBF16Out, kKind>;
+  static_assert(sizeof(Smem<kKind>) + 1024 <= 227 * 1024, "shared memory per CTA");
+  const size_t smem = sizeof(Smem<kKind>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -394,7 +453,7 @@ cudaError_t launch_variant(const MxGemmArgs& a, int num_sms, cudaStream_t s) {
                        (a.out_bf16 ? (a.N % 8 == 0) : (a.N % 4 == 0));
   return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, s, a.tmA, a.tmB,
                     a.sfA, a.sfB, a.C, a.D, a.M, a.N, a.K, static_cast<uint32_t>(a.afmt),
-                    static_cast<uint32_t>(a.bfmt), vec_out, raster_n);
+                    static_cast<uint32_t>(a.bfmt), vec_out, raster_n, a.alpha);
 }
 
 }  // namespace
@@ -411,8 +470,25 @@ cudaError_t gemm_mx_error_read_and_clear(cudaStream_t s, uint32_t* out) {
 
 int gemm_mx_b_box_rows() { return BN; }
 
+bool gemm_mx_fp4_large(int M, int N, int num_sms) {
+  // the 128 x 256 kernel once there are at least half as many tiles as SMs;
+  // smaller FP4 problems keep the 128 x 128 general kernel (more CTAs)
+  const int64_t tiles = (static_cast<int64_t>(M) + BM - 1) / BM * ((N + BN - 1) / BN);
+  return tiles >= num_sms / 2;
+}
+
 cudaError_t launch_gemm_mx(const MxGemmArgs& a, int num_sms, cudaStream_t s) {
-  return a.out_bf16 ? launch_variant<true>(a, num_sms, s) : launch_variant<false>(a, num_sms, s);
+  switch (a.kind) {
+    case kMxfp4:
+      return a.out_bf16 ? launch_variant<true, kMxfp4>(a, num_sms, s)
+                        : launch_variant<false, kMxfp4>(a, num_sms, s);
+    case kNvfp4:
+      return a.out_bf16 ? launch_variant<true, kNvfp4>(a, num_sms, s)
+                        : launch_variant<false, kNvfp4>(a, num_sms, s);
+    default:
+      return a.out_bf16 ? launch_variant<true, kMxfp8>(a, num_sms, s)
+                        : launch_variant<false, kMxfp8>(a, num_sms, s);
+  }
 }
 
 }  // namespace bsg

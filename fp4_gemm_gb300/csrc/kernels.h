@@ -82,10 +82,14 @@ bool gemm_fp8_use_pair(int M, int N, int num_sms);
 int gemm_fp8_b_box_rows(bool pair);
 cudaError_t launch_gemm_fp8(const Fp8GemmArgs& a, int num_sms, cudaStream_t s);
 
-// MXFP8 GEMM (FP8 operands, E8M0 scales per 32 along K in the tcgen05 layout).
+// Block-scaled GEMM for large shapes (128 x 256 tiles): MXFP8 (FP8 operands,
+// E8M0 per 32), MXFP4 (packed E2M1, E8M0 per 32) or NVFP4 (packed E2M1, E4M3
+// per 16, times alpha); scales in the tcgen05 layout.
 struct MxGemmArgs {
   int M, N, K;
-  int afmt, bfmt;            // 0 E4M3, 1 E5M2
+  int kind;                  // 0 MXFP8, 1 MXFP4, 2 NVFP4
+  float alpha;               // NVFP4: the sum is multiplied by alpha
+  int afmt, bfmt;            // MXFP8: 0 E4M3, 1 E5M2
   const uint8_t* sfA;
   const uint8_t* sfB;
   const float* C;
@@ -94,6 +98,8 @@ struct MxGemmArgs {
   CUtensorMap tmA, tmB;      // A: box 128 B x 128 rows; B: box 128 B x gemm_mx_b_box_rows()
 };
 int gemm_mx_b_box_rows();
+// Whether an FP4 problem takes this kernel rather than the general FP4 one.
+bool gemm_mx_fp4_large(int M, int N, int num_sms);
 cudaError_t launch_gemm_mx(const MxGemmArgs& a, int num_sms, cudaStream_t s);
 
 struct Mxfp4GemmArgs {

@@ -91,3 +91,34 @@ def test_decode_full_size_sampled_columns(M):
     Dref, bnd = og.gemm_mxfp4(opa, ofa, opb, ofb)
     Dg = D.float().cpu().numpy()[:, cols]
     report(f"decode full size M={M} ({cols.size} columns)", *og.within_tolerance(Dg, Dref, bnd, bf16=True))
+
+
+# Shapes with at least half as many 128 x 256 tiles as SMs take the large
+# block-scaled kernel: ragged M and N, an N whose last tile holds one 128-row
+# scale block (1900), K tails that leave a partial stage and a partial atom.
+@pytest.mark.parametrize("M,N,K,out,addend", [(2000, 2000, 288, "f32", False),
+                                              (1300, 1900, 1056, "bf16", True)])
+def test_mxfp4_large_kernel_ragged(M, N, K, out, addend):
+    A, B = synth.make("mxfp4_1024", m=M, n=N, k=K)
+    C = synth.addend("mxfp4_1024", M, N) if addend else None
+    rows = np.unique(np.concatenate([np.arange(0, M, 7), [M - 1]]))
+    report(f"mxfp4 large {M}x{N}x{K}", *_run(A, B, out, C=C, rows=rows))
+
+
+def test_mxfp4_large_kernel_ffn_up_shape_sampled():
+    import fp4_gemm_gb300 as bsg
+    dev = device()
+    _, M, N, K = synth.WORKLOADS["ffn_up"]
+    A, B = synth.make("ffn_up")
+    pa, fa = bsg.bsg_quantize_mxfp4(to_dev(A, dev), "tcgen05")
+    pb, fb = bsg.bsg_quantize_mxfp4(to_dev(B, dev), "tcgen05")
+    D = bsg.bsg_gemm(pa, "e2m1", fa, "mx", pb, "e2m1", fb, "mx", out="bf16")
+    assert bsg.bsg_device_error() == 0
+    g = np.random.default_rng(13)
+    rows = np.unique(np.concatenate([[0, 127, 128, M - 1], g.integers(0, M, 28)]))
+    cols = np.unique(np.concatenate([[0, 255, 256, N - 1], g.integers(0, N, 60)]))
+    opa, ofa = oq.quantize_mxfp4(A[rows])      # MX scales are per row: rows quantise alone
+    opb, ofb = oq.quantize_mxfp4(B[cols])
+    Dref, bnd = og.gemm_mxfp4(opa, ofa, opb, ofb)
+    report("mxfp4 ffn_up sampled", *og.within_tolerance(D.float().cpu().numpy()[np.ix_(rows, cols)],
+                                                        Dref, bnd, bf16=True))

@@ -88,3 +88,18 @@ def test_nvfp4_gemm_ffn_up_full_size_sampled():
     rows = np.unique(np.concatenate([[0, 127, 128, M - 1], g.integers(0, M, 28)]))
     cols = np.unique(np.concatenate([[0, 127, 128, N - 1], g.integers(0, N, 60)]))
     report("nvfp4 ffn_up sampled", *_gemm(M, N, K, ga=1.0, gb=2.0 ** -6, out="bf16", rows=rows, cols=cols))
+
+
+@pytest.mark.parametrize("M,N,K,out,addend", [(2000, 2000, 288, "f32", False),
+                                              (1300, 1900, 1056, "bf16", True)])
+def test_nvfp4_large_kernel_ragged(M, N, K, out, addend):
+    # at least half as many 128 x 256 tiles as SMs: the large block-scaled
+    # kernel (three stages of four scale atoms), partial last stage and atom
+    rows = np.unique(np.concatenate([np.arange(0, M, 7), [M - 1]]))
+    report(f"nvfp4 large {M}x{N}x{K}", *_gemm(M, N, K, ga=2.0 ** -1, gb=2.0 ** -6, out=out,
+                                              addend=addend, rows=rows))
+
+
+def test_nvfp4_large_kernel_through_bsg_gemm():
+    report("nvfp4 large via bsg_gemm", *_gemm(1536, 2048, 512, ga=1.0, gb=1.0, via_bsg_gemm=True,
+                                              rows=np.arange(0, 1536, 5)))
