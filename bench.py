@@ -70,7 +70,7 @@ L2_BYTES = 129 << 20
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {"fp8": ["gemm_fp8.cu", "common.cuh", "quant_math.cuh"], "fp4": ["gemm_mxfp4.cu", "common.cuh"],
-                  "mx8": ["gemm_mx.cu", "common.cuh"]}
+                  "mx": ["gemm_mx.cu", "common.cuh"]}
 # workloads that reuse another workload's shape and seeded inputs
 SHAPE_OF = {"mxfp8_ffn_up": "ffn_up", "ffn_up_q8out": "ffn_up", "nvfp4_ffn_up": "ffn_up"}
 
@@ -618,8 +618,9 @@ def main():
         dt = "fp4" if (w.fp4 or w.nv4) else "fp8"
         achieved = w.flops() / g_s / 1e12
         peak = pk["bf16_tflops"] * RATIO[dt]
-        src_kind = "mx8" if w.mx8 else dt
-        kernel = "gemm_mxfp4_kernel" if (w.fp4 or w.nv4) else ("gemm_mx_kernel" if w.mx8 else "gemm_fp8_kernel")
+        # MXFP8 and the large NVFP4 GEMM run the 128 x 256 block-scaled kernel
+        src_kind = "mx" if (w.mx8 or w.nv4) else dt
+        kernel = "gemm_mxfp4_kernel" if w.fp4 else ("gemm_mx_kernel" if (w.mx8 or w.nv4) else "gemm_fp8_kernel")
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": measured_traffic(w.name, src_kind),
                 "kernel": kernel,
