@@ -33,7 +33,8 @@ LAYOUT = {"rowmajor": 0, "tcgen05": 1}
 EXPORTS = ("bsg_quantize_fp8", "bsg_quantize_mxfp4", "bsg_gemm", "bsg_gemm_workspace_size",
            "bsg_scale_bytes", "bsg_sf_to_tcgen05", "bsg_status_string", "bsg_device_error",
            "bsg_num_sms", "bsg_gemm_decode_noalloc", "bsg_mma_peak", "bsg_quantize_mx",
-           "bsg_mma_probe", "bsg_gemm_quantized", "bsg_quantize_nvfp4", "bsg_gemm_nvfp4")
+           "bsg_mma_probe", "bsg_gemm_quantized", "bsg_quantize_nvfp4", "bsg_gemm_nvfp4",
+           "bsg_check_wait_timeout")
 
 
 class BsgError(RuntimeError):
@@ -85,6 +86,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsg_quantize_nvfp4.restype = i32
     lib.bsg_gemm_nvfp4.argtypes = [i64, i64, i64, vp, vp, vp, vp, f32, vp, vp, i32, vp]
     lib.bsg_gemm_nvfp4.restype = i32
+    lib.bsg_check_wait_timeout.argtypes = [vp]
+    lib.bsg_check_wait_timeout.restype = i32
     lib.bsg_mma_peak.argtypes = [i32, i32, i32, i64, c.POINTER(i64), vp]
     lib.bsg_mma_probe.argtypes = [vp, i32, vp, i32, vp, vp, vp]
     lib.bsg_mma_probe.restype = i32
@@ -155,6 +158,13 @@ def bsg_mma_probe(A: torch.Tensor, fa: str, B: torch.Tensor, fb: str, C: torch.T
 
 def bsg_status_string(status: int) -> str:
     return load_library().bsg_status_string(status).decode()
+
+
+def bsg_check_wait_timeout(stream=None) -> None:
+    """Launch the failure-detection self-check: a kernel whose only wait runs
+    out after the library's limit.  The next bsg_device_error() returns
+    BSG_ERR_TIMEOUT (5)."""
+    _check(load_library().bsg_check_wait_timeout(_stream(stream)), "bsg_check_wait_timeout")
 
 
 def bsg_device_error(stream=None) -> int:

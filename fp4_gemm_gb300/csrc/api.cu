@@ -465,18 +465,23 @@ bsg_status bsg_quantize_nvfp4(const void* x, bsg_dtype src, int64_t rows, int64_
                                               static_cast<cudaStream_t>(stream)));
 }
 
+bsg_status bsg_check_wait_timeout(void* stream) {
+  return from_cuda(bsg::launch_wait_timeout_check(static_cast<cudaStream_t>(stream)));
+}
+
 bsg_status bsg_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return BSG_ERR_CUDA;
-  uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0, w4 = 0, w5 = 0;
+  uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0, w4 = 0, w5 = 0, w6 = 0;
   if (bsg::quantize_error_read_and_clear(s, &w0) != cudaSuccess ||
       bsg::gemm_fp8_error_read_and_clear(s, &w1) != cudaSuccess ||
       bsg::gemm_mxfp4_error_read_and_clear(s, &w2) != cudaSuccess ||
       bsg::mma_peak_error_read_and_clear(s, &w3) != cudaSuccess ||
       bsg::gemm_mx_error_read_and_clear(s, &w4) != cudaSuccess ||
-      bsg::mma_probe_error_read_and_clear(s, &w5) != cudaSuccess)
+      bsg::mma_probe_error_read_and_clear(s, &w5) != cudaSuccess ||
+      bsg::watchdog_error_read_and_clear(s, &w6) != cudaSuccess)
     return BSG_ERR_CUDA;
-  const uint32_t w = w0 | w1 | w2 | w3 | w4 | w5;
+  const uint32_t w = w0 | w1 | w2 | w3 | w4 | w5 | w6;
   if (w & 1u) return BSG_ERR_TIMEOUT;
   if (w & 2u) return BSG_ERR_WORKSPACE;
   return BSG_OK;

@@ -134,5 +134,8 @@ cudaError_t launch_mma_peak(int kind, bool pair, int64_t iters, int num_sms, cud
 // (row-major device arrays; fmt 0 E4M3, 1 E5M2).
 cudaError_t launch_mma_probe(const uint8_t* A, int afmt, const uint8_t* B, int bfmt, const float* C,
                              float* D, cudaStream_t s);
+// A kernel whose only wait runs out (the failure-detection self-check).
+cudaError_t launch_wait_timeout_check(cudaStream_t s);
+cudaError_t watchdog_error_read_and_clear(cudaStream_t s, uint32_t* out);
 
 }  // namespace bsg

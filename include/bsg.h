@@ -355,6 +355,18 @@ bsg_status bsg_mma_probe(const uint8_t* A, bsg_format fa, const uint8_t* B, bsg_
 /* Human-readable name of a status. */
 const char* bsg_status_string(bsg_status status);
 
+/* bsg_check_wait_timeout - self-check of the failure detection.
+ *
+ * Every wait inside the library's kernels is bounded (2 s); a wait that runs
+ * out is reported by bsg_device_error as BSG_ERR_TIMEOUT and the kernel
+ * returns instead of hanging or trapping.  This call launches one small
+ * kernel whose only wait is on a barrier nothing arrives on, so the wait
+ * runs out after the limit: the next bsg_device_error returns
+ * BSG_ERR_TIMEOUT (and clears it), and the context stays usable.
+ * Errors: BSG_ERR_CUDA (launch failure).
+ */
+bsg_status bsg_check_wait_timeout(void* stream);
+
 /* Synchronise `stream`, then read and clear the device error word.  Returns
  * BSG_OK, BSG_ERR_TIMEOUT if a kernel's bounded wait ran out since the last
  * call, or BSG_ERR_CUDA if the synchronisation itself failed. */
