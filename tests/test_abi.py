@@ -53,3 +53,38 @@ def test_invalid_arguments_rejected_before_launch():
     assert lib.bsg_gemm(4, 4, 32, 24, 0, 16, 0, 16, 0, 16, 0, None, 16, 0, None, 0, None) == 3
     assert lib.bsg_gemm(4, 4, 32, 16, 0, 16, 0, 16, 2, 16, 2, None, 16, 0, None, 0, None) == 2
     assert lib.bsg_sf_to_tcgen05(None, 1, 1, None, None) == 1
+
+
+def test_newer_entry_points_reject_bad_arguments_before_launch():
+    import fp4_gemm_gb300 as bsg
+    lib = bsg.load_library()
+    f32 = 0
+    e4m3, e5m2, e2m1 = 0, 1, 2
+    tile, row, mx, nv = 0, 1, 2, 3
+    # bsg_gemm_quantized: null output, E2M1 output format, mixed-in MX
+    # scales, fmt_max above 2^64, K % 16, misaligned scales
+    args = [256, 256, 256, 16, e4m3, 16, row, 16, e4m3, 16, tile, None]
+    assert lib.bsg_gemm_quantized(*args, e4m3, 0.0, None, 16, None) == 1
+    assert lib.bsg_gemm_quantized(*args, e2m1, 0.0, 16, 16, None) == 2
+    assert lib.bsg_gemm_quantized(256, 256, 256, 16, e4m3, 16, mx, 16, e4m3, 16, mx, None,
+                                  e4m3, 0.0, 16, 16, None) == 2
+    assert lib.bsg_gemm_quantized(*args, e5m2, 2.0 ** 65, 16, 16, None) == 1
+    assert lib.bsg_gemm_quantized(256, 256, 24, 16, e4m3, 16, row, 16, e4m3, 16, tile, None,
+                                  e4m3, 0.0, 16, 16, None) == 1
+    assert lib.bsg_gemm_quantized(*args, e4m3, 0.0, 16, 18, None) == 3
+    # bsg_quantize_nvfp4: null, cols % 16, bad tensor scale, misaligned codes
+    assert lib.bsg_quantize_nvfp4(None, f32, 4, 32, 32, 1.0, 16, 16, 0, None) == 1
+    assert lib.bsg_quantize_nvfp4(16, f32, 4, 40, 40, 1.0, 16, 16, 0, None) == 1
+    assert lib.bsg_quantize_nvfp4(16, f32, 4, 32, 32, 0.0, 16, 16, 0, None) == 1
+    assert lib.bsg_quantize_nvfp4(16, f32, 4, 32, 32, float("inf"), 16, 16, 0, None) == 1
+    assert lib.bsg_quantize_nvfp4(16, f32, 4, 32, 32, 1.0, 18, 16, 0, None) == 3
+    # bsg_gemm_nvfp4: K % 32, non-finite alpha, misaligned scales
+    assert lib.bsg_gemm_nvfp4(4, 4, 48, 16, 16, 16, 16, 1.0, None, 16, f32, None) == 1
+    assert lib.bsg_gemm_nvfp4(4, 4, 64, 16, 16, 16, 16, float("nan"), None, 16, f32, None) == 1
+    assert lib.bsg_gemm_nvfp4(4, 4, 64, 16, 24, 16, 16, 1.0, None, 16, f32, None) == 3
+    # bsg_gemm: NVFP4 scales on one operand only
+    assert lib.bsg_gemm(4, 4, 64, 16, e2m1, 16, nv, 16, e2m1, 16, mx, None, 16, f32, None, 0, None) == 2
+    # scale sizes of the 1 x 16 E4M3 granularity
+    assert bsg.bsg_scale_bytes(130, 96, "nv", "rowmajor") == 130 * 6
+    assert bsg.bsg_scale_bytes(130, 96, "nv", "tcgen05") == 2 * 2 * 512
+    assert bsg.bsg_scale_bytes(10, 40, "nv", "rowmajor") == 0
