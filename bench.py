@@ -285,7 +285,8 @@ class Clocks:
     def __init__(self, gpu_index):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        import tempfile
+        self.path = os.path.join(tempfile.gettempdir(), f"bsg_clocks_bench_{os.getpid()}.csv")
 
     def start(self):
         try:
