@@ -58,6 +58,33 @@ struct GroupDiv {
   }
 };
 
+// Four FP8 codes of x / s (s = d.s), each quotient correctly rounded to FP32
+// first: the codes of cvt4_fp8(fmt, RN(a/s), RN(b/s), RN(c/s), RN(e/s)).
+// The range test is taken once for the four.  In range, Markstein's steps
+// give RN(x/s) whenever |x/s| >= 2^-18; smaller quotients are an FP8 zero
+// whichever way they round, so each code's sign bit is taken from its x
+// (a quotient of x by a positive s has x's sign) and GroupDiv's per-element
+// zero fix-up is not needed.
+__device__ __forceinline__ uint32_t fp8_codes4(int fmt, const GroupDiv& d, float a, float b, float c,
+                                               float e) {
+  float q[4] = {a, b, c, e};
+  if (d.fast) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float x = q[i];
+      float t = x * d.r;
+      t = fmaf(fmaf(-t, d.s, x), d.r, t);
+      q[i] = fmaf(fmaf(-t, d.s, x), d.r, t);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = __fdiv_rn(q[i], d.s);
+  }
+  const uint32_t sg = __byte_perm(__byte_perm(__float_as_uint(a), __float_as_uint(b), 0x0073),
+                                  __byte_perm(__float_as_uint(c), __float_as_uint(e), 0x0073), 0x5410);
+  return (cvt4_fp8(fmt, q[0], q[1], q[2], q[3]) & 0x7F7F7F7Fu) | (sg & 0x80808080u);
+}
+
 // E8M0 code of the power of two nearest to v >= 0 (ties up), from v's bits.
 __device__ __forceinline__ uint32_t e8m0_nearest(float v) {
   const uint32_t b = __float_as_uint(v);

@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kTileThreads) quantize_fp8_tile_kernel(
   for (int i = 0; i < kTileRowsPerThread; ++i) {
     const int64_t row = r0 + rr + kWarps * i;
     if (row < rows && col < cols) {
-      const uint32_t c = cvt4_fp8(fmt, div(v[i][0]), div(v[i][1]), div(v[i][2]), div(v[i][3]));
+      const uint32_t c = fp8_codes4(fmt, div, v[i][0], v[i][1], v[i][2], v[i][3]);
       store_codes4(q, row * cols + col, col, cols, vec_out, c);
     }
   }
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) quantize_fp8_row_kernel(
     if (lane == 0) scales[t * rows + row] = s;
     if (col < cols) {
       const GroupDiv div(s, r);
-      const uint32_t c = cvt4_fp8(fmt, div(v[i][0]), div(v[i][1]), div(v[i][2]), div(v[i][3]));
+      const uint32_t c = fp8_codes4(fmt, div, v[i][0], v[i][1], v[i][2], v[i][3]);
       store_codes4(q, row * cols + col, col, cols, vec_out, c);
     }
   }
