@@ -22,7 +22,10 @@
 // Two kernels:
 //  * gemm_mxfp4_kernel: 128 x 128 output tiles, persistent, warp-specialised
 //    (TMA producer warp, MMA warp, 8 epilogue warps draining a double-
-//    buffered accumulator).
+//    buffered accumulator).  It also runs NVFP4 (kNv: UE4M3 scales per 16,
+//    kind::mxf4nvf4 scale_vec::4X, the sum times alpha).  It serves problems
+//    with few tiles; larger FP4 problems go to the 128 x 256 block-scaled
+//    kernel of gemm_mx.cu.
 //  * gemm_mxfp4_decode_kernel: decode shapes (M <= 32 activation rows).  The
 //    weights are the MMA's 128-row operand and the activations its N = 16/32
 //    operand ("swap AB"), so the weight matrix streams from HBM exactly once.
