@@ -136,6 +136,30 @@ def test_tcgen05_layout_is_a_permutation():
     assert sorted(out.tolist()) == sorted(sf.ravel().tolist() + [127] * (out.size - sf.size))
 
 
+def test_tcgen05_layout_hand_placed_bytes():
+    # The tensor core's scale-factor atom (NVIDIA's PTX ISA, tcgen05 block
+    # scaling; the same 128 x 4 tile as cuBLAS's block-scaling layout): 512
+    # bytes per 128 rows x 4 K-blocks, stored as [32][4][4] = (row mod 32,
+    # row / 32 within the 128, K-block mod 4); atoms ordered row block major.
+    # Each expected offset below is worked out by hand from that description.
+    R, KB = 256, 8                 # 2 row blocks x 2 atoms along K
+    placed = {                     # (row, K-block): offset in bytes
+        (0, 0): 0, (1, 0): 16, (31, 0): 496, (32, 0): 4, (96, 0): 12,
+        (0, 1): 1, (0, 3): 3, (33, 2): 22, (127, 3): 511,
+        (0, 4): 512, (5, 6): 594,          # second atom of row block 0
+        (128, 0): 1024,                    # first atom of row block 1
+        (200, 7): 1675,                    # 1536 + 8*16 + 2*4 + 3
+    }
+    sf = np.zeros((R, KB), np.uint8)
+    for n, (r, c) in enumerate(placed):
+        sf[r, c] = n + 1
+    out = quantize.sf_to_tcgen05_layout(sf)
+    assert out.size == 4 * 512
+    for n, off in enumerate(placed.values()):
+        assert out[off] == n + 1, (off, out[off])
+    assert np.count_nonzero(out) == len(placed)
+
+
 def test_mxfp8_hand_worked_e4m3():
     # E4M3 max 448.  Block max 448 -> v = 1 -> 2^0; 672 -> v = 1.5 -> tie -> 2^1;
     # 600 -> v = 1.34 -> 2^0 (600 saturates to 448); 0 -> code 127.
