@@ -267,7 +267,9 @@ bsg_status bsg_sf_to_tcgen05(const uint8_t* sf_rowmajor, int64_t rows, int64_t k
 }
 
 size_t bsg_gemm_workspace_size(int64_t M, int64_t N, int64_t K, bsg_format fa, bsg_format fb) {
-  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  // sizes bsg_gemm would reject need no workspace (and must not reach the
+  // int arithmetic of the plan)
+  if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return 0;
   if (fa == BSG_E2M1 && fb == BSG_E2M1 && M <= kDecodeMaxM) {
     const int sms = num_sms_current();
     return bsg::gemm_mxfp4_decode_workspace(static_cast<int>(M), static_cast<int>(N),

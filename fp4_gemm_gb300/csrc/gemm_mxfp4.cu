@@ -390,7 +390,7 @@ Plan make_plan(int M, int N, int K, int num_sms) {
   Plan p;
   p.nx = M <= 16 ? 16 : 32;
   p.ch = chunks_for(K, p.nx);
-  p.tiles = (N + 127) / 128;
+  p.tiles = (static_cast<int64_t>(N) + 127) / 128;
   p.KS = (static_cast<int64_t>(K) / 2 + kRowBytes * p.ch - 1) / (kRowBytes * p.ch);
   p.U = p.tiles * p.KS;
   p.G = p.U < num_sms ? p.U : num_sms;

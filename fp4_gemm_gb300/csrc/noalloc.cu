@@ -14,7 +14,10 @@
 // library holds kNoallocScratchBytes of it until the process exits.  Host
 // code cannot use the variable's name as a device address, so the address is
 // fetched with cudaGetSymbolAddress, once per device, with that device
-// current, on the first call made on it.
+// current, on the first call made on it.  The address is kept for the life
+// of the process: a cudaDeviceReset (or any teardown of the device's primary
+// context) after that first call is not supported, since the kept address
+// would then point into a context that no longer exists.
 #include <mutex>
 
 #include "bsg.h"
@@ -24,6 +27,7 @@
 namespace {
 
 constexpr size_t kNoallocScratchBytes = size_t{8} << 20;  // 8 MiB
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
 constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
@@ -51,18 +55,24 @@ extern "C" bsg_status bsg_gemm_decode_noalloc(int64_t M, int64_t N, int64_t K, c
                                               const void* sA, const void* B, const void* sB,
                                               const float* C, void* D, bsg_dtype out,
                                               void* stream) {
+  if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return BSG_ERR_INVALID_ARG;
   if (M > 32) return BSG_ERR_UNSUPPORTED;
   const size_t need = bsg_gemm_workspace_size(M, N, K, BSG_E2M1, BSG_E2M1);
   if (need > kNoallocScratchBytes) return BSG_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (need > 0) {
-    if (M <= 0 || N <= 0 || K <= 0) return BSG_ERR_INVALID_ARG;
     scratch = scratch_on_current_device();
     if (scratch == nullptr) return BSG_ERR_CUDA;
-    // The counters that must start at zero sit after the partial-sum slots;
-    // clearing the whole used span also covers a previous call that stopped
-    // early and left it dirty.
-    if (cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    // The split-K scratch is the partial-sum slots followed by one 32-bit
+    // counter per 128-row weight tile.  Only the counters must start at zero:
+    // a tile's partials are summed once its counter shows that every
+    // contributor of this call has written its slot, so a slot is never read
+    // before this call wrote it, whatever an earlier call (even one that
+    // stopped early) left there.
+    const size_t counter_bytes = static_cast<size_t>((N + 127) / 128) * sizeof(uint32_t);
+    if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + (need - counter_bytes), 0,
+                        counter_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return BSG_ERR_CUDA;
   }
   return bsg_gemm(M, N, K, A, BSG_E2M1, sA, BSG_SCALE_BLOCK1x32_E8M0, B, BSG_E2M1, sB,

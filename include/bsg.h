@@ -302,8 +302,11 @@ bsg_status bsg_sf_to_tcgen05(const uint8_t* sf_rowmajor, int64_t rows, int64_t k
  * every GPU that loads libbsg.so holds it until the process exits.  The
  * first call on a device looks up the array's device address (with that
  * device current), so make that first call before any stream capture.
- * Each call clears the part it uses (an asynchronous memset on `stream`)
- * and then runs the decode kernel; nothing is allocated.  All calls share
+ * Each call clears the per-tile counters that must start at zero (an
+ * asynchronous memset on `stream`) and then runs the decode kernel; nothing
+ * is allocated.  The looked-up address is kept for the process's lifetime,
+ * so cudaDeviceReset after the first call on a device is not supported.
+ * All calls share
  * the one array: calls whose execution overlaps on the GPU (different
  * streams, or different host threads) race and give wrong results.
  * Errors: as bsg_gemm; BSG_ERR_UNSUPPORTED if M > 32; BSG_ERR_WORKSPACE if
