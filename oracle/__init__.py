@@ -8,12 +8,17 @@ the two share no code, tables or constants.  Inputs come from ``synth``.
 Contents (each function cites the passage it follows):
 
 * ``formats``  bit-field decoders and round-to-nearest-even encoders for FP8
-               E4M3 (fn) / E5M2, FP4 E2M1 and the E8M0 scale.
+               E4M3 (fn) / E5M2, FP4 E2M1, the E8M0 scale and the BF16 / FP16
+               block scales.
 * ``quantize`` the per-tile FP8 quantiser (scale = max_abs / format max), the
                MXFP4 quantiser (E8M0 per 32 elements along K, nibble packing)
-               and the MXFP8 quantiser (the same MX rule with FP8 elements).
+               the MXFP8 quantiser (the same MX rule with FP8 elements), the
+               NVFP4 quantiser and the FP4 quantiser with a BF16 / FP16 scale
+               per 32 elements along K.
 * ``gemm``     D = sum_k (s_A a_k)(s_B b_k) + C in FP64, with the per-element
-               error bound sum_k |s_A a_k s_B b_k| used by the tolerance.
+               error bound sum_k |s_A a_k s_B b_k| used by the tolerance, and
+               step-by-step emulations of the promoted GEMMs (FP8 per 128-wide
+               K tile; FP4 with 16-bit scales per 32-wide K block).
 * ``fda``      the Hopper FP8 MMA bit model (aligned truncated sum, RZ-E8M13)
                used only to interpret hardware results, never as the
                correctness reference.
