@@ -27,14 +27,14 @@ STATUS = {0: "BSG_OK", 1: "BSG_ERR_INVALID_ARG", 2: "BSG_ERR_UNSUPPORTED", 3: "B
           4: "BSG_ERR_CUDA", 5: "BSG_ERR_TIMEOUT", 6: "BSG_ERR_WORKSPACE"}
 FORMAT = {"e4m3": 0, "e5m2": 1, "e2m1": 2}
 DTYPE = {"f32": 0, "bf16": 1}
-GRAN = {"tile": 0, "row": 1, "mx": 2, "nv": 3}
+GRAN = {"tile": 0, "row": 1, "mx": 2, "nv": 3, "bf16": 4, "f16": 5}
 LAYOUT = {"rowmajor": 0, "tcgen05": 1}
 
 EXPORTS = ("bsg_quantize_fp8", "bsg_quantize_mxfp4", "bsg_gemm", "bsg_gemm_workspace_size",
            "bsg_scale_bytes", "bsg_sf_to_tcgen05", "bsg_status_string", "bsg_device_error",
            "bsg_num_sms", "bsg_gemm_decode_noalloc", "bsg_mma_peak", "bsg_quantize_mx",
            "bsg_mma_probe", "bsg_gemm_quantized", "bsg_quantize_nvfp4", "bsg_gemm_nvfp4",
-           "bsg_check_wait_timeout")
+           "bsg_check_wait_timeout", "bsg_quantize_fp4_bs16")
 
 
 class BsgError(RuntimeError):
@@ -84,6 +84,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsg_quantize_mx.restype = i32
     lib.bsg_quantize_nvfp4.argtypes = [vp, i32, i64, i64, i64, f32, vp, vp, i32, vp]
     lib.bsg_quantize_nvfp4.restype = i32
+    lib.bsg_quantize_fp4_bs16.argtypes = [vp, i32, i64, i64, i64, i32, vp, vp, vp]
+    lib.bsg_quantize_fp4_bs16.restype = i32
     lib.bsg_gemm_nvfp4.argtypes = [i64, i64, i64, vp, vp, vp, vp, f32, vp, vp, i32, vp]
     lib.bsg_gemm_nvfp4.restype = i32
     lib.bsg_check_wait_timeout.argtypes = [vp]
@@ -272,6 +274,27 @@ def bsg_quantize_nvfp4(x: torch.Tensor, layout: str = "tcgen05", tensor_scale: f
     _check(lib.bsg_quantize_nvfp4(_ptr(x), src, rows, cols, x.stride(0), float(tensor_scale),
                                   _ptr(q), _ptr(sf), LAYOUT[layout], _stream(stream)),
            "bsg_quantize_nvfp4")
+    return q, sf
+
+
+def bsg_quantize_fp4_bs16(x: torch.Tensor, scale: str = "bf16", q: torch.Tensor | None = None,
+                          sf: torch.Tensor | None = None, stream=None):
+    """E2M1 quantisation with one 16-bit scale ("bf16" or "f16") per 32 along K,
+    x: (rows, K) FP32 or BF16 CUDA tensor, K % 32 == 0.  Returns (packed uint8
+    (rows, K/2), scale codes int16 (K/32, rows)); pass scale as the
+    granularity of both operands to bsg_gemm."""
+    lib = load_library()
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D tensor with unit column stride")
+    rows, cols = x.shape
+    src = {torch.float32: 0, torch.bfloat16: 1}[x.dtype]
+    if q is None:
+        q = torch.empty((rows, cols // 2), dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sf = torch.empty((cols // 32, rows), dtype=torch.int16, device=x.device)
+    _need_cuda(x, q, sf)
+    _check(lib.bsg_quantize_fp4_bs16(_ptr(x), src, rows, cols, x.stride(0), GRAN[scale], _ptr(q),
+                                     _ptr(sf), _stream(stream)), "bsg_quantize_fp4_bs16")
     return q, sf
 
 

@@ -110,6 +110,21 @@ bool make_kmajor_map_chunked(CUtensorMap* map, const void* base, uint64_t inner_
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_fp4_unpack_map(CUtensorMap* map, const void* base, uint64_t K, uint64_t rows,
+                         uint64_t pitch, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || K % 128 != 0 || pitch % 32 != 0 ||
+      reinterpret_cast<uintptr_t>(base) % 32 != 0)
+    return false;
+  cuuint64_t dims[2] = {K, rows};               // in 4-bit values
+  cuuint64_t strides[1] = {pitch};              // bytes
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace bsg
 
 using bsg::make_kmajor_map;
@@ -204,6 +219,10 @@ size_t bsg_scale_bytes(int64_t rows, int64_t cols, bsg_scale_gran gran, bsg_sf_l
       if (layout == BSG_SF_TCGEN05)
         return static_cast<size_t>(cdiv(rows, 128) * cdiv(cols / 16, 4) * 512);
       return static_cast<size_t>(rows * (cols / 16));
+    case BSG_SCALE_BLOCK1x32_BF16:
+    case BSG_SCALE_BLOCK1x32_F16:
+      if (cols % 32) return 0;
+      return static_cast<size_t>((cols / 32) * rows) * sizeof(uint16_t);
   }
   return 0;
 }
@@ -342,9 +361,17 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
   } else {
     const bool mx = ga == BSG_SCALE_BLOCK1x32_E8M0 && gb == BSG_SCALE_BLOCK1x32_E8M0;
     const bool nv = ga == BSG_SCALE_BLOCK1x16_E4M3 && gb == BSG_SCALE_BLOCK1x16_E4M3;
-    if (!mx && !nv) return BSG_ERR_UNSUPPORTED;
-    if (K % 32) return BSG_ERR_INVALID_ARG;
-    if (!aligned(sA, 16) || !aligned(sB, 16)) return BSG_ERR_ALIGNMENT;
+    const bool bs16 = (ga == BSG_SCALE_BLOCK1x32_BF16 || ga == BSG_SCALE_BLOCK1x32_F16) && gb == ga;
+    if (!mx && !nv && !bs16) return BSG_ERR_UNSUPPORTED;
+    if (bs16) {
+      // the unpacking tensor maps need K % 128 == 0 and 32-byte aligned rows
+      if (K % 128) return BSG_ERR_INVALID_ARG;
+      if (!aligned(A, 32) || !aligned(B, 32) || !aligned(sA, 2) || !aligned(sB, 2))
+        return BSG_ERR_ALIGNMENT;
+    } else {
+      if (K % 32) return BSG_ERR_INVALID_ARG;
+      if (!aligned(sA, 16) || !aligned(sB, 16)) return BSG_ERR_ALIGNMENT;
+    }
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int sms = num_sms_current();
@@ -375,6 +402,24 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
     a.D = D;
     a.out_bf16 = out == BSG_BF16;
     return run_fp8(&a, A, B, out == BSG_BF16 ? 2 : 4, sms, s);
+  }
+  if (ga == BSG_SCALE_BLOCK1x32_BF16 || ga == BSG_SCALE_BLOCK1x32_F16) {
+    bsg::Bs16GemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.f16_scales = ga == BSG_SCALE_BLOCK1x32_F16;
+    a.sfA = static_cast<const uint16_t*>(sA);
+    a.sfB = static_cast<const uint16_t*>(sB);
+    a.C = C;
+    a.D = D;
+    a.out_bf16 = out == BSG_BF16;
+    a.vec_out = aligned(D, 16) && N % (out == BSG_BF16 ? 8 : 4) == 0;
+    if (!bsg::make_fp4_unpack_map(&a.tmA, A, K, M, K / 2, 128) ||
+        !bsg::make_fp4_unpack_map(&a.tmB, B, K, N, K / 2, 256))
+      return BSG_ERR_CUDA;
+    return from_cuda(bsg::launch_gemm_bs16(a, sms, s));
   }
   {
     Mxfp4GemmArgs a;
@@ -471,19 +516,35 @@ bsg_status bsg_check_wait_timeout(void* stream) {
   return from_cuda(bsg::launch_wait_timeout_check(static_cast<cudaStream_t>(stream)));
 }
 
+bsg_status bsg_quantize_fp4_bs16(const void* x, bsg_dtype src, int64_t rows, int64_t cols,
+                                 int64_t ld, bsg_scale_gran gran, uint8_t* q_packed, uint16_t* sf,
+                                 void* stream) {
+  if (x == nullptr || q_packed == nullptr || sf == nullptr) return BSG_ERR_INVALID_ARG;
+  if (rows <= 0 || cols <= 0 || ld < cols || rows > kMaxDim || cols > kMaxDim || cols % 32)
+    return BSG_ERR_INVALID_ARG;
+  if (src != BSG_F32 && src != BSG_BF16) return BSG_ERR_INVALID_ARG;
+  if (gran != BSG_SCALE_BLOCK1x32_BF16 && gran != BSG_SCALE_BLOCK1x32_F16) return BSG_ERR_UNSUPPORTED;
+  if (!aligned(x, src == BSG_F32 ? 4 : 2) || !aligned(q_packed, 4) || !aligned(sf, 2))
+    return BSG_ERR_ALIGNMENT;
+  return from_cuda(bsg::launch_quantize_fp4_bs16(x, src == BSG_BF16, rows, cols, ld,
+                                                 gran == BSG_SCALE_BLOCK1x32_F16, q_packed, sf,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
 bsg_status bsg_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return BSG_ERR_CUDA;
-  uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0, w4 = 0, w5 = 0, w6 = 0;
+  uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0, w4 = 0, w5 = 0, w6 = 0, w7 = 0;
   if (bsg::quantize_error_read_and_clear(s, &w0) != cudaSuccess ||
       bsg::gemm_fp8_error_read_and_clear(s, &w1) != cudaSuccess ||
       bsg::gemm_mxfp4_error_read_and_clear(s, &w2) != cudaSuccess ||
       bsg::mma_peak_error_read_and_clear(s, &w3) != cudaSuccess ||
       bsg::gemm_mx_error_read_and_clear(s, &w4) != cudaSuccess ||
       bsg::mma_probe_error_read_and_clear(s, &w5) != cudaSuccess ||
-      bsg::watchdog_error_read_and_clear(s, &w6) != cudaSuccess)
+      bsg::watchdog_error_read_and_clear(s, &w6) != cudaSuccess ||
+      bsg::gemm_bs16_error_read_and_clear(s, &w7) != cudaSuccess)
     return BSG_ERR_CUDA;
-  const uint32_t w = w0 | w1 | w2 | w3 | w4 | w5 | w6;
+  const uint32_t w = w0 | w1 | w2 | w3 | w4 | w5 | w6 | w7;
   if (w & 1u) return BSG_ERR_TIMEOUT;
   if (w & 2u) return BSG_ERR_WORKSPACE;
   return BSG_OK;

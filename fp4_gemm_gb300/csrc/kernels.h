@@ -123,6 +123,32 @@ cudaError_t launch_gemm_mxfp4(const Mxfp4GemmArgs& a, int num_sms, cudaStream_t 
 size_t gemm_mxfp4_decode_workspace(int M, int N, int K, int num_sms);
 cudaError_t launch_gemm_mxfp4_decode(const Mxfp4GemmArgs& a, int num_sms, cudaStream_t s);
 
+// FP4 GEMM with a BF16 or FP16 scale per 32 along K (codes [K/32][rows]),
+// promoted per K block.  A and B are packed E2M1 (rows x K/2 bytes); their
+// tensor maps use the 16U4_ALIGN16B type (box 128 elements x 128 / 256 rows).
+struct Bs16GemmArgs {
+  int M, N, K;               // K % 128 == 0
+  bool f16_scales;           // FP16 scale codes (else BF16)
+  const uint16_t* sfA;
+  const uint16_t* sfB;
+  const float* C;
+  void* D;
+  bool out_bf16;
+  bool vec_out;              // D is 16-byte aligned and rows are whole 16-byte pieces
+  CUtensorMap tmA, tmB;
+};
+cudaError_t launch_gemm_bs16(const Bs16GemmArgs& a, int num_sms, cudaStream_t s);
+cudaError_t gemm_bs16_error_read_and_clear(cudaStream_t s, uint32_t* out);
+// 2-D map of a packed E2M1 matrix (rows x K values, row pitch `pitch` bytes)
+// that unpacks on load (16U4_ALIGN16B): box 128 values x box_rows, 128-byte
+// swizzle.  Needs K % 128 == 0, a 32-byte aligned base and pitch % 32 == 0.
+bool make_fp4_unpack_map(CUtensorMap* map, const void* base, uint64_t K, uint64_t rows,
+                         uint64_t pitch, uint32_t box_rows);
+// FP4 quantiser with a BF16 / FP16 scale per 32 along K (codes [K/32][rows]).
+cudaError_t launch_quantize_fp4_bs16(const void* x, bool src_bf16, int64_t rows, int64_t cols,
+                                     int64_t ld, bool f16_scales, uint8_t* q, uint16_t* sf,
+                                     cudaStream_t s);
+
 // ------------------------------------------------- tensor-core microbenchmark
 // Back-to-back tcgen05.mma from shared memory on every SM; *flops receives
 // the floating-point operations the launch performs.  kind: 0 dense FP8,
