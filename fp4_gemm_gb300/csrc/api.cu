@@ -417,7 +417,8 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
     a.out_bf16 = out == BSG_BF16;
     a.vec_out = aligned(D, 16) && N % (out == BSG_BF16 ? 8 : 4) == 0;
     if (!bsg::make_fp4_unpack_map(&a.tmA, A, K, M, K / 2, 128) ||
-        !bsg::make_fp4_unpack_map(&a.tmB, B, K, N, K / 2, 256))
+        !bsg::make_fp4_unpack_map(&a.tmB, B, K, N, K / 2,
+                                  static_cast<uint32_t>(bsg::gemm_bs16_b_box_rows())))
       return BSG_ERR_CUDA;
     return from_cuda(bsg::launch_gemm_bs16(a, sms, s));
   }

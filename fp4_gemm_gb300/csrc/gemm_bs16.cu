@@ -28,22 +28,27 @@
 // 4-byte tensor-memory read and two FP32 operations (the scale product and
 // the FMA), against 64 tensor-core FLOPs.  The FP32 pipe (128 lanes per SM)
 // therefore bounds the kernel near a quarter of the FP8 MMA rate; the
-// tensor core idles most of the time.  Hence a simple structure:
+// tensor core idles most of the time.  What matters is keeping the FP32
+// pipe fed: three drain warps per SM sub-partition, each with 64 columns
+// (64 accumulators), so one warp's waits and load latencies overlap the
+// others' arithmetic.
 //
-// Warp roles (384 threads, one CTA per SM, persistent over 128 x 256 tiles):
-//   warp 0     producer: TMA loads of A (128 rows) and B (256 rows), one
+// Warp roles (512 threads, one CTA per SM, persistent over 128 x 192 tiles):
+//   warp 0     producer: TMA loads of A (128 rows) and B (192 rows), one
 //              128-element K stage at a time, into a 4-stage ring.
 //   warp 1     tensor-memory allocator; MMA issuer (one lane): per K block
-//              one M128 N256 K32 MMA into buffer (block & 1), a commit to
+//              one M128 N192 K32 MMA into buffer (block & 1), a commit to
 //              that buffer's pfull barrier, and after a stage's fourth block
 //              a commit to the stage's done barrier.
 //   warp 2     scale loader: each stage's A and B block scales (16-bit codes,
-//              [K/32][rows] in global memory) converted to FP32 into a
-//              3-slot shared-memory ring.
-//   warps 4-11 drain + epilogue: warp w drains TMEM lanes 32 (w % 4) .. +31
-//              (its rows) and column half (w - 4) / 4 of the 256-wide tile,
-//              128 FP32 accumulators per thread; after the last block the
-//              thread adds C and stores its 128 outputs.
+//              [K/32][rows] in global memory) into a 4-slot shared-memory
+//              ring, by bulk copies when the rows are whole 16-byte pieces
+//              (else by plain loads); the drain warps convert the codes as
+//              they use them.
+//   warps 4-15 drain + epilogue: warp w drains TMEM lanes 32 (w % 4) .. +31
+//              (its rows) and column group (w - 4) / 4 (64 columns) of the
+//              192-wide tile into 64 FP32 accumulators per thread; after the
+//              last block the thread adds C and stores its 64 outputs.
 // Every wait is bounded; a wait that runs out sets the error word, raises a
 // CTA-wide abort flag and every role unwinds to the final barrier.
 #include <cuda_fp16.h>
@@ -57,22 +62,25 @@ namespace {
 __device__ uint32_t g_bs16_error = 0;
 
 constexpr int BM = 128;             // output rows per tile
-constexpr int BN = 256;             // output columns per tile
+constexpr int BN = 192;             // output columns per tile
+constexpr int kGroupCols = 64;      // columns per drain warp
 constexpr int BKS = 128;            // K elements per shared-memory stage
 constexpr int KBLK = 32;            // K elements per scale block = per MMA
 constexpr int kBlocksPerStage = BKS / KBLK;
 constexpr int kStages = 4;
-constexpr int kScaleSlots = 3;
-constexpr int kThreads = 384;
+constexpr int kScaleSlots = 4;
+constexpr int kThreads = 512;
+constexpr int kDrainWarps = 12;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kScaleWarp = 2;
 constexpr int kFirstDrainWarp = 4;
 constexpr int kRegsSmall = 56;
-constexpr int kRegsLarge = 224;
-static_assert(128 * kRegsSmall + 256 * kRegsLarge <= kThreads * 168,
+constexpr int kRegsLarge = 152;
+static_assert(128 * kRegsSmall + 32 * kDrainWarps * kRegsLarge <= kThreads * 128,
               "register split exceeds the launch allocation");
-constexpr int kTmemCols = 512;      // two 256-column FP32 partial buffers
+constexpr int kTmemCols = 512;      // two 192-column FP32 partial buffers
+constexpr int kBufStride = 256;     // buffer b starts at column 256 b
 constexpr int kGroup = 8;           // tile raster: groups of 8 tiles along M
 
 // Bytes the TMA moves per stage: the packed operands (half a byte per
@@ -82,8 +90,8 @@ constexpr uint32_t kStageTxBytes = (BM + BN) * BKS / 2;
 struct __align__(1024) Smem {
   uint8_t a[kStages][BM * BKS];       // unpacked: 128 bytes per row per stage
   uint8_t b[kStages][BN * BKS];
-  float sa[kScaleSlots][kBlocksPerStage][BM];
-  float sb[kScaleSlots][kBlocksPerStage][BN];
+  uint16_t sa[kScaleSlots][kBlocksPerStage][BM];     // scale codes as stored in global memory
+  uint16_t sb[kScaleSlots][kBlocksPerStage][BN];
   uint64_t full[kStages];
   uint64_t done[kStages];             // the stage's MMAs completed: slot free
   uint64_t pfull[2];                  // partial of the block in buffer b ready
@@ -115,13 +123,29 @@ __device__ __forceinline__ void raise_abort(volatile uint32_t* flag) {
   *flag = 1u;
 }
 
-// Value of a 16-bit scale code: BF16 (the top half of an FP32) or FP16.
+// Scale codes to FP32, exactly.  A BF16 code is the top half of an FP32.
+// An FP16 code (non-negative) moved into FP32's exponent/mantissa position
+// reads as its value times 2^-112, subnormals included (the FP16 exponent
+// field lines up with FP32's, and a zero exponent field gives an FP32
+// subnormal with the same significand).  So for FP16 the row scale carries
+// the factor 2^112 (at most 65504 * 2^112 < 2^128, no overflow) and the
+// column scales carry 2^-112: their product is the exact s_A * s_B, rounded
+// once by the multiply, as for BF16.
 template <bool kF16>
-__device__ __forceinline__ float scale_value(uint16_t c) {
+__device__ __forceinline__ float row_scale(uint32_t c) {
   if constexpr (kF16)
-    return __half2float(__ushort_as_half(c));
+    return __fmul_rn(__fmul_rn(__uint_as_float((c & 0x7FFFu) << 13), 0x1p112f), 0x1p112f);
   else
-    return __uint_as_float(static_cast<uint32_t>(c) << 16);
+    return __uint_as_float(c << 16);
+}
+// Two column scales from one 32-bit word of codes (first column in the low
+// half), as an FP32 pair (FP16: times 2^-112).
+template <bool kF16>
+__device__ __forceinline__ uint64_t col_scale_pair(uint32_t w) {
+  if constexpr (kF16)
+    return f32x2_pack(__uint_as_float((w & 0x7FFFu) << 13), __uint_as_float((w >> 3) & 0x0FFFE000u));
+  else
+    return f32x2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
 template <bool kF16, bool kBF16Out>
@@ -129,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_bs16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const uint16_t* __restrict__ sfA, const uint16_t* __restrict__ sfB,
                      const float* __restrict__ Cin, void* __restrict__ Dout, int M, int N, int K,
-                     uint32_t idesc, bool vec_out) {
+                     uint32_t idesc, bool vec_out, bool bulk_scales) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~static_cast<uintptr_t>(1023));
@@ -149,11 +173,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&sm.pfull[b]), 1);
-      mbar_init(smem_u32(&sm.tempty[b]), 8);
+      mbar_init(smem_u32(&sm.tempty[b]), kDrainWarps);
     }
     for (int s = 0; s < kScaleSlots; ++s) {
-      mbar_init(smem_u32(&sm.sfull[s]), 32);
-      mbar_init(smem_u32(&sm.sempty[s]), 8);
+      mbar_init(smem_u32(&sm.sfull[s]), 1);
+      mbar_init(smem_u32(&sm.sempty[s]), kDrainWarps);
     }
     mbar_init(smem_u32(&sm.final_bar), 1);
     sm.abort_flag = 0u;
@@ -233,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          mma_f8f6f4(tmem + b * BN, ad + 2 * kk, bd + 2 * kk, idesc, 0u);
+          mma_f8f6f4(tmem + b * kBufStride, ad + 2 * kk, bd + 2 * kk, idesc, 0u);
           tc_commit(smem_u32(&sm.pfull[b]));
         }
         if (!ok) break;
@@ -246,16 +270,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kScaleWarp) {
     // ------------------------------------------------------- scale loader
-    // Stage it's scales: A's 4 blocks x 128 rows and B's 4 blocks x 256
-    // rows, 16-bit codes at [kb][row] (consecutive lanes read consecutive
-    // rows), converted to FP32; rows past M / N read as 0 (their partials are
-    // 0 as well).  Every lane arrives on sfull after its own stores.
+    // Stage it's scale codes: A's 4 blocks x 128 rows and B's 4 blocks x 192
+    // rows, [kb][row] in global memory, into slot it % kScaleSlots once the
+    // drains have released it.  With whole 16-byte rows (M, N multiples of
+    // 8) one bulk copy per block and operand, completing on sfull; else plain
+    // loads (codes past M / N become 0) and an arrive after them.
     setmaxnreg_dec<kRegsSmall>();
+    for (int i = lane; i < kScaleSlots * kBlocksPerStage * (BM + BN) / 2; i += 32)
+      reinterpret_cast<uint32_t*>(&sm.sa[0][0][0])[i] = 0u;     // sa and sb are contiguous
+    fence_proxy_async_smem();   // before bulk copies overwrite them
+    __syncwarp();
     uint32_t it = 0;
     bool ok = true;
     for (int t = unit; t < tiles && ok; t += units) {
       const TileCoord tc = tile_coord(t, num_m, num_n);
       const int m0 = tc.m * BM, n0 = tc.n * BN;
+      const int na = min(BM, M - m0), nb = min(BN, N - n0);
       for (int kt = 0; kt < KT; ++kt, ++it) {
         if (sm.abort_flag) { ok = false; break; }
         const int ss = static_cast<int>(it % kScaleSlots);
@@ -266,23 +296,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         good = __shfl_sync(0xffffffffu, good, 0);
         if (!good) { ok = false; break; }
-#pragma unroll 4
-        for (int i = lane; i < kBlocksPerStage * BM; i += 32) {
-          const int kk = i / BM, r = i % BM;
-          const int64_t kb = static_cast<int64_t>(kt) * kBlocksPerStage + kk;
-          const int row = m0 + r;
-          sm.sa[ss][kk][r] = row < M ? scale_value<kF16>(__ldg(sfA + kb * M + row)) : 0.0f;
+        if (bulk_scales) {
+          if (lane == 0) {
+            fence_proxy_async_smem();   // the drains' reads of the slot come first
+            const uint32_t bar = smem_u32(&sm.sfull[ss]);
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(kBlocksPerStage * (na + nb) * 2));
+#pragma unroll
+            for (int kk = 0; kk < kBlocksPerStage; ++kk) {
+              const int64_t kb = static_cast<int64_t>(kt) * kBlocksPerStage + kk;
+              bulk_load(smem_u32(sm.sa[ss][kk]), sfA + kb * M + m0, static_cast<uint32_t>(na * 2), bar);
+              bulk_load(smem_u32(sm.sb[ss][kk]), sfB + kb * N + n0, static_cast<uint32_t>(nb * 2), bar);
+            }
+          }
+        } else {
+          for (int i = lane; i < kBlocksPerStage * BM; i += 32) {
+            const int kk = i / BM, r = i % BM;
+            const int64_t kb = static_cast<int64_t>(kt) * kBlocksPerStage + kk;
+            sm.sa[ss][kk][r] = r < na ? __ldg(sfA + kb * M + m0 + r) : static_cast<uint16_t>(0);
+          }
+          for (int i = lane; i < kBlocksPerStage * BN; i += 32) {
+            const int kk = i / BN, c = i % BN;
+            const int64_t kb = static_cast<int64_t>(kt) * kBlocksPerStage + kk;
+            sm.sb[ss][kk][c] = c < nb ? __ldg(sfB + kb * N + n0 + c) : static_cast<uint16_t>(0);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm.sfull[ss]));
         }
-#pragma unroll 4
-        for (int i = lane; i < kBlocksPerStage * BN; i += 32) {
-          const int kk = i / BN, c = i % BN;
-          const int64_t kb = static_cast<int64_t>(kt) * kBlocksPerStage + kk;
-          const int col = n0 + c;
-          sm.sb[ss][kk][c] = col < N ? scale_value<kF16>(__ldg(sfB + kb * N + col)) : 0.0f;
-        }
-        mbar_arrive(smem_u32(&sm.sfull[ss]));
       }
     }
+    // no bulk copy may still be landing when the CTA exits
+    if (bulk_scales && lane == 0)
+      for (uint32_t j = it > kScaleSlots ? it - kScaleSlots : 0u; j < it; ++j)
+        if (!mbar_wait(smem_u32(&sm.sfull[j % kScaleSlots]), (j / kScaleSlots) & 1u)) break;
     (void)KB;
     __syncwarp();
   } else if (warp < kFirstDrainWarp) {
@@ -293,17 +338,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------- drain + epilogue
     setmaxnreg_inc<kRegsLarge>();
     const int q = warp & 3;                        // TMEM lane quarter = rows 32q..32q+31
-    const int g = (warp - kFirstDrainWarp) >> 2;   // column half of the 256-wide tile
+    const int g = (warp - kFirstDrainWarp) >> 2;   // 64-column group of the tile
     const int row = q * 32 + lane;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + g * 128;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + g * kGroupCols;
     uint32_t it = 0;
     bool ok = true;
     for (int t = unit; t < tiles && ok; t += units) {
       if (sm.abort_flag) break;
       const TileCoord tc = tile_coord(t, num_m, num_n);
-      uint64_t acc[64];                            // 128 FP32 accumulators, in pairs
+      uint64_t acc[kGroupCols / 2];                // 64 FP32 accumulators, in pairs
 #pragma unroll
-      for (int j = 0; j < 64; ++j) acc[j] = 0ull;
+      for (int i = 0; i < kGroupCols / 2; ++i) acc[i] = 0ull;
       for (int kt = 0; kt < KT && ok; ++kt, ++it) {
         const int ss = static_cast<int>(it % kScaleSlots);
         if (!mbar_wait(smem_u32(&sm.sfull[ss]), (it / kScaleSlots) & 1u)) {
@@ -320,36 +365,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const float sa = sm.sa[ss][kk][row];
+          const uint32_t taddr = lane_base + b * kBufStride;
+          // both 32-column loads in flight at once; the buffer goes back to
+          // the MMA as soon as they have landed
+          uint32_t r0[32], r1[32];
+          tmem_ld_32(taddr, r0);
+          tmem_ld_32(taddr + 32, r1);
+          const float sa = row_scale<kF16>(sm.sa[ss][kk][row]);
           const uint64_t sa2 = f32x2_pack(sa, sa);
-          const float* sbp = &sm.sb[ss][kk][g * 128];
-          const uint32_t taddr = lane_base + b * BN;
-          // 16 columns per tcgen05.ld, double-buffered; the buffer goes back
-          // to the MMA as soon as its last load has landed
-          uint32_t r0[16], r1[16];
-          tmem_ld_16(taddr, r0);
-          tc_wait_ld_16(r0);
+          const uint16_t* sbp = &sm.sb[ss][kk][g * kGroupCols];
+          tc_wait_ld_32(r0);
+          tc_wait_ld_32(r1);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm.tempty[b]));
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t (&cur)[16] = (c & 1) ? r1 : r0;
-            uint32_t (&nxt)[16] = (c & 1) ? r0 : r1;
-            if (c + 1 < 8) tmem_ld_16(taddr + (c + 1) * 16, nxt);
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t (&cur)[32] = c ? r1 : r0;
 #pragma unroll
-            for (int jj = 0; jj < 8; jj += 2) {
-              const int pi = c * 8 + jj;           // pair index = column / 2
-              const float4 sbv = *reinterpret_cast<const float4*>(sbp + 2 * pi);
-              const uint64_t s01 = fmul2(sa2, f32x2_pack(sbv.x, sbv.y));
-              const uint64_t s23 = fmul2(sa2, f32x2_pack(sbv.z, sbv.w));
-              ffma2(acc[pi], s01, f32x2_pack(__uint_as_float(cur[2 * jj]), __uint_as_float(cur[2 * jj + 1])));
-              ffma2(acc[pi + 1], s23,
-                    f32x2_pack(__uint_as_float(cur[2 * jj + 2]), __uint_as_float(cur[2 * jj + 3])));
-            }
-            if (c + 1 < 8) tc_wait_ld_16(nxt);
-            if (c == 6) {
-              // every tcgen05.ld of this buffer has completed
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(smem_u32(&sm.tempty[b]));
+            for (int v = 0; v < 4; ++v) {          // 8 columns: one 16-byte load of codes
+              const uint4 w = *reinterpret_cast<const uint4*>(sbp + c * 32 + v * 8);
+              const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int jj = v * 4 + e;          // pair within the chunk
+                const uint64_t sc = fmul2(sa2, col_scale_pair<kF16>(wv[e]));
+                ffma2(acc[c * 16 + jj], sc,
+                      f32x2_pack(__uint_as_float(cur[2 * jj]), __uint_as_float(cur[2 * jj + 1])));
+              }
             }
           }
         }
@@ -358,13 +401,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&sm.sempty[ss]));   // scales used
       }
       if (!ok) break;
-      // ---- epilogue: this thread's row x 128 columns, + C, straight to D
+      // ---- epilogue: this thread's row x 64 columns, + C, straight to D
       const int64_t grow = static_cast<int64_t>(tc.m) * BM + row;
-      const int gcol0 = tc.n * BN + g * 128;
+      const int gcol0 = tc.n * BN + g * kGroupCols;
       if (grow < M) {
         constexpr int kPer = kBF16Out ? 8 : 4;     // values per 16-byte store
 #pragma unroll
-        for (int c = 0; c < 128 / kPer; ++c) {
+        for (int c = 0; c < kGroupCols / kPer; ++c) {
           float v[kPer];
 #pragma unroll
           for (int e = 0; e < kPer / 2; ++e) f32x2_unpack(acc[c * (kPer / 2) + e], v[2 * e], v[2 * e + 1]);
@@ -419,9 +462,12 @@ cudaError_t launch_variant(const Bs16GemmArgs& a, int num_sms, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
-  const uint32_t idesc = idesc_f8f6f4(5u, 5u, BM, BN);   // E2M1 x E2M1, M128 N256
+  const uint32_t idesc = idesc_f8f6f4(5u, 5u, BM, BN);   // E2M1 x E2M1, M128 N192
+  // bulk copies of scale rows need 16-byte aligned rows: M, N multiples of 8
+  const bool bulk = a.M % 8 == 0 && a.N % 8 == 0 && reinterpret_cast<uintptr_t>(a.sfA) % 16 == 0 &&
+                    reinterpret_cast<uintptr_t>(a.sfB) % 16 == 0;
   return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, s, a.tmA, a.tmB,
-                    a.sfA, a.sfB, a.C, a.D, a.M, a.N, a.K, idesc, a.vec_out);
+                    a.sfA, a.sfB, a.C, a.D, a.M, a.N, a.K, idesc, a.vec_out, bulk);
 }
 
 }  // namespace
@@ -435,6 +481,8 @@ cudaError_t gemm_bs16_error_read_and_clear(cudaStream_t s, uint32_t* out) {
   if (e != cudaSuccess) return e;
   return cudaStreamSynchronize(s);
 }
+
+int gemm_bs16_b_box_rows() { return BN; }
 
 cudaError_t launch_gemm_bs16(const Bs16GemmArgs& a, int num_sms, cudaStream_t s) {
   if (a.f16_scales)

@@ -125,7 +125,8 @@ cudaError_t launch_gemm_mxfp4_decode(const Mxfp4GemmArgs& a, int num_sms, cudaSt
 
 // FP4 GEMM with a BF16 or FP16 scale per 32 along K (codes [K/32][rows]),
 // promoted per K block.  A and B are packed E2M1 (rows x K/2 bytes); their
-// tensor maps use the 16U4_ALIGN16B type (box 128 elements x 128 / 256 rows).
+// tensor maps use the 16U4_ALIGN16B type (box 128 elements x 128 rows for A,
+// gemm_bs16_b_box_rows() for B).
 struct Bs16GemmArgs {
   int M, N, K;               // K % 128 == 0
   bool f16_scales;           // FP16 scale codes (else BF16)
@@ -138,6 +139,7 @@ struct Bs16GemmArgs {
   CUtensorMap tmA, tmB;
 };
 cudaError_t launch_gemm_bs16(const Bs16GemmArgs& a, int num_sms, cudaStream_t s);
+int gemm_bs16_b_box_rows();        // B rows per tile (the B map's box height)
 cudaError_t gemm_bs16_error_read_and_clear(cudaStream_t s, uint32_t* out);
 // 2-D map of a packed E2M1 matrix (rows x K values, row pitch `pitch` bytes)
 // that unpacks on load (16U4_ALIGN16B): box 128 values x box_rows, 128-byte

@@ -11,7 +11,7 @@ sys.path.insert(0, ROOT)
 import bench  # noqa: E402
 
 WORKLOADS = ["ffn_up", "dgrad", "decode", "fp8_256", "mxfp4_1024", "mxfp8_ffn_up", "ffn_up_q8out",
-             "nvfp4_ffn_up"]
+             "nvfp4_ffn_up", "bs16_ffn_up"]
 
 
 @pytest.mark.parametrize("name", WORKLOADS)
