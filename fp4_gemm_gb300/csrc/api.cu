@@ -177,8 +177,9 @@ bsg_status run_fp4_large(int kind, float alpha, int64_t M, int64_t N, int64_t K,
   a.C = C;
   a.D = D;
   a.out_bf16 = out_bf16;
+  a.pair = bsg::gemm_mx_use_pair(a.M, a.N, sms);
   if (!make_kmajor_map(&a.tmA, A, K / 2, M, K / 2, 128) ||
-      !make_kmajor_map(&a.tmB, B, K / 2, N, K / 2, static_cast<uint32_t>(bsg::gemm_mx_b_box_rows())))
+      !make_kmajor_map(&a.tmB, B, K / 2, N, K / 2, static_cast<uint32_t>(bsg::gemm_mx_b_box_rows(a.pair))))
     return BSG_ERR_CUDA;
   return from_cuda(bsg::launch_gemm_mx(a, sms, s));
 }
@@ -390,8 +391,9 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
     a.C = C;
     a.D = D;
     a.out_bf16 = out == BSG_BF16;
+    a.pair = bsg::gemm_mx_use_pair(a.M, a.N, sms);
     if (!make_kmajor_map(&a.tmA, A, K, M, K, 128) ||
-        !make_kmajor_map(&a.tmB, B, K, N, K, static_cast<uint32_t>(bsg::gemm_mx_b_box_rows())))
+        !make_kmajor_map(&a.tmB, B, K, N, K, static_cast<uint32_t>(bsg::gemm_mx_b_box_rows(a.pair))))
       return BSG_ERR_CUDA;
     return from_cuda(bsg::launch_gemm_mx(a, sms, s));
   }

@@ -95,9 +95,12 @@ struct MxGemmArgs {
   const float* C;
   void* D;
   bool out_bf16;
-  CUtensorMap tmA, tmB;      // A: box 128 B x 128 rows; B: box 128 B x gemm_mx_b_box_rows()
+  bool pair;                 // CTA-pair kernel (256 x 256 tiles, tcgen05 cta_group::2)
+  CUtensorMap tmA, tmB;      // A: box 128 B x 128 rows; B: box 128 B x gemm_mx_b_box_rows(pair)
 };
-int gemm_mx_b_box_rows();
+int gemm_mx_b_box_rows(bool pair);
+// Whether a large block-scaled problem takes the CTA-pair kernel.
+bool gemm_mx_use_pair(int M, int N, int num_sms);
 // Whether an FP4 problem takes this kernel rather than the general FP4 one.
 bool gemm_mx_fp4_large(int M, int N, int num_sms);
 cudaError_t launch_gemm_mx(const MxGemmArgs& a, int num_sms, cudaStream_t s);
