@@ -34,7 +34,7 @@ EXPORTS = ("bsg_quantize_fp8", "bsg_quantize_mxfp4", "bsg_gemm", "bsg_gemm_works
            "bsg_scale_bytes", "bsg_sf_to_tcgen05", "bsg_status_string", "bsg_device_error",
            "bsg_num_sms", "bsg_gemm_decode_noalloc", "bsg_mma_peak", "bsg_quantize_mx",
            "bsg_mma_probe", "bsg_gemm_quantized", "bsg_quantize_nvfp4", "bsg_gemm_nvfp4",
-           "bsg_check_wait_timeout", "bsg_quantize_fp4_bs16")
+           "bsg_check_wait_timeout", "bsg_quantize_fp4_bs16", "bsg_mma_probe_mx")
 
 
 class BsgError(RuntimeError):
@@ -93,6 +93,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsg_mma_peak.argtypes = [i32, i32, i32, i64, c.POINTER(i64), vp]
     lib.bsg_mma_probe.argtypes = [vp, i32, vp, i32, vp, vp, vp]
     lib.bsg_mma_probe.restype = i32
+    lib.bsg_mma_probe_mx.argtypes = [i32, vp, vp, vp, vp, vp, vp, i32, i32, vp]
+    lib.bsg_mma_probe_mx.restype = i32
     lib.bsg_mma_peak.restype = i32
     _lib = lib
     return lib
@@ -155,6 +157,25 @@ def bsg_mma_probe(A: torch.Tensor, fa: str, B: torch.Tensor, fb: str, C: torch.T
     _need_cuda(A, B, C, D)
     _check(load_library().bsg_mma_probe(_ptr(A), FORMAT[fa], _ptr(B), FORMAT[fb], _ptr(C), _ptr(D),
                                         _stream(stream)), "bsg_mma_probe")
+    return D
+
+
+def bsg_mma_probe_mx(kind: int, A: torch.Tensor, sfA: torch.Tensor, B: torch.Tensor,
+                     sfB: torch.Tensor, C: torch.Tensor, fa: str = "e4m3", fb: str = "e4m3",
+                     stream=None) -> torch.Tensor:
+    """One block-scaled MMA (kind 0 MXFP8, 1 MXFP4, 2 NVFP4): returns D
+    (128, 256) float32 from operand bytes A (128, 32), B (256, 32), scale
+    cells sfA (128, 4), sfB (256, 4) (uint8) and C (128, 256)."""
+    if (A.shape != (128, 32) or B.shape != (256, 32) or sfA.shape != (128, 4) or
+            sfB.shape != (256, 4) or C.shape != (128, 256)):
+        raise ValueError("bsg_mma_probe_mx takes A (128,32), B (256,32), sfA (128,4), sfB (256,4), C (128,256)")
+    A, B, sfA, sfB = A.contiguous(), B.contiguous(), sfA.contiguous(), sfB.contiguous()
+    C = C.contiguous().float()
+    D = torch.empty((128, 256), dtype=torch.float32, device=A.device)
+    _need_cuda(A, B, sfA, sfB, C, D)
+    _check(load_library().bsg_mma_probe_mx(kind, _ptr(A), _ptr(sfA), _ptr(B), _ptr(sfB), _ptr(C),
+                                           _ptr(D), FORMAT[fa], FORMAT[fb], _stream(stream)),
+           "bsg_mma_probe_mx")
     return D
 
 

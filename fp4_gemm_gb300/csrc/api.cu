@@ -519,6 +519,19 @@ bsg_status bsg_check_wait_timeout(void* stream) {
   return from_cuda(bsg::launch_wait_timeout_check(static_cast<cudaStream_t>(stream)));
 }
 
+bsg_status bsg_mma_probe_mx(int kind, const uint8_t* A, const uint8_t* sfA, const uint8_t* B,
+                           const uint8_t* sfB, const float* C, float* D, bsg_format fa,
+                           bsg_format fb, void* stream) {
+  if (A == nullptr || sfA == nullptr || B == nullptr || sfB == nullptr || C == nullptr ||
+      D == nullptr || kind < 0 || kind > 2)
+    return BSG_ERR_INVALID_ARG;
+  if (kind == 0 && (!is_fp8(fa) || !is_fp8(fb))) return BSG_ERR_UNSUPPORTED;
+  if (!aligned(sfA, 4) || !aligned(sfB, 4) || !aligned(C, 4) || !aligned(D, 4))
+    return BSG_ERR_ALIGNMENT;
+  return from_cuda(bsg::launch_mma_probe_mx(kind, A, sfA, B, sfB, C, D, fa == BSG_E5M2 ? 1 : 0,
+                                            fb == BSG_E5M2 ? 1 : 0, static_cast<cudaStream_t>(stream)));
+}
+
 bsg_status bsg_quantize_fp4_bs16(const void* x, bsg_dtype src, int64_t rows, int64_t cols,
                                  int64_t ld, bsg_scale_gran gran, uint8_t* q_packed, uint16_t* sf,
                                  void* stream) {

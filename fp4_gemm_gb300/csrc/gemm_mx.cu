@@ -467,14 +467,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < kPerPiece; ++j) {
             const int col = ch * kColsPerChunk + p * kPerPiece + j;
             v[j] = __uint_as_float(r[col / 32][col % 32]);
-            if (kKind == kNvfp4) v[j] *= alpha;
           }
-          if (Cin != nullptr && my_row < M) {
+          // alpha * acc + C with one rounding (NVFP4), acc + C otherwise:
+          // written out so that the compiler's contraction choices do not
+          // decide the result bits
+          const bool add_c = Cin != nullptr && my_row < M;
 #pragma unroll
-            for (int j = 0; j < kPerPiece; ++j) {
-              const int col = col0 + p * kPerPiece + j;
-              if (col < N) v[j] += __ldg(Cin + my_row * N + col);
-            }
+          for (int j = 0; j < kPerPiece; ++j) {
+            const int col = col0 + p * kPerPiece + j;
+            const float c = (add_c && col < N) ? __ldg(Cin + my_row * N + col) : 0.0f;
+            if (kKind == kNvfp4)
+              v[j] = add_c ? __fmaf_rn(v[j], alpha, c) : __fmul_rn(v[j], alpha);
+            else if (add_c)
+              v[j] = __fadd_rn(v[j], c);
           }
           uint4 u;
           if (kBF16Out) {

@@ -264,14 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-          if (kNv) {
+          // alpha * acc + C with one rounding (NVFP4), acc + C otherwise:
+          // written out so that the compiler's contraction choices do not
+          // decide the result bits
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] *= alpha;
-          }
-          if (Cin != nullptr) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (col + j < N) v[j] += __ldg(Cin + grow * N + col + j);
+          for (int j = 0; j < 16; ++j) {
+            const float c = (Cin != nullptr && col + j < N) ? __ldg(Cin + grow * N + col + j) : 0.0f;
+            if (kNv)
+              v[j] = Cin != nullptr ? __fmaf_rn(v[j], alpha, c) : __fmul_rn(v[j], alpha);
+            else if (Cin != nullptr)
+              v[j] = __fadd_rn(v[j], c);
           }
           if (kBF16Out) {
             __nv_bfloat16* D = static_cast<__nv_bfloat16*>(Dout) + grow * N;

@@ -165,6 +165,13 @@ cudaError_t launch_mma_peak(int kind, bool pair, int64_t iters, int num_sms, cud
 // (row-major device arrays; fmt 0 E4M3, 1 E5M2).
 cudaError_t launch_mma_probe(const uint8_t* A, int afmt, const uint8_t* B, int bfmt, const float* C,
                              float* D, cudaStream_t s);
+// One block-scaled tcgen05.mma of the GEMMs' shape (M128 N256): kind 0
+// kind::mxf8f6f4 1X (FP8 formats afmt / bfmt), 1 kind::mxf4 2X, 2
+// kind::mxf4nvf4 4X.  A [128][32] / B [256][32] operand bytes as in shared
+// memory, sfA [128][4] / sfB [256][4] scale cells, C / D [128][256] FP32.
+cudaError_t launch_mma_probe_mx(int kind, const uint8_t* A, const uint8_t* sfA, const uint8_t* B,
+                                const uint8_t* sfB, const float* C, float* D, int afmt, int bfmt,
+                                cudaStream_t s);
 // A kernel whose only wait runs out (the failure-detection self-check).
 cudaError_t launch_wait_timeout_check(cudaStream_t s);
 cudaError_t watchdog_error_read_and_clear(cudaStream_t s, uint32_t* out);

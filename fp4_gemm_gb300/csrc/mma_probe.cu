@@ -91,7 +91,118 @@ __global__ void __launch_bounds__(128, 1)
   }
 }
 
+// The block-scaled kinds, one MMA of the GEMMs' own shape (M128 N256) and
+// scale layout: D[128][256] = sum over the instruction's K of
+// (sA a)(sB b) + C, with the scale bytes given per row as the four bytes of
+// the row's tensor-memory scale cell (kind 0: kind::mxf8f6f4 scale_vec::1X,
+// K = 32, byte 0; kind 1: kind::mxf4 scale_vec::2X, K = 64, bytes 0-1;
+// kind 2: kind::mxf4nvf4 scale_vec::4X, K = 64, UE4M3 bytes 0-3).  A row's
+// 32 operand bytes (32 FP8 values or 64 packed E2M1) are given as they sit in
+// shared memory.
+constexpr int XN = 256;
+constexpr uint32_t kXScaleA = 256;       // scale columns after the accumulator
+constexpr uint32_t kXScaleB = 264;       // B's two 128-row blocks: +0..3 and +4..7
+
+__global__ void __launch_bounds__(128, 1)
+    mma_probe_mx_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ sfA,
+                        const uint8_t* __restrict__ B, const uint8_t* __restrict__ sfB,
+                        const float* __restrict__ C, float* __restrict__ D, int kind, uint32_t idesc) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sa = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* sb = sa + PM * 128;
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tslot;
+  const int warp = static_cast<int>(warp_id());
+  const int lane = static_cast<int>(lane_id());
+  for (int i = threadIdx.x; i < (PM + XN) * 128 / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(sa)[i] = make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+  for (int i = threadIdx.x; i < PM * 32; i += blockDim.x) sa[swz128(i / 32, i % 32)] = A[i];
+  for (int i = threadIdx.x; i < XN * 32; i += blockDim.x) sb[swz128(i / 32, i % 32)] = B[i];
+  fence_proxy_async_smem();
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tslot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tslot;
+  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  // the accumulator: this warp's 32 rows x 256 columns of C
+  const int row = warp * 32 + lane;
+  for (int c0 = 0; c0 < XN; c0 += 16) {
+    uint32_t c[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) c[j] = __float_as_uint(C[row * XN + c0 + j]);
+    tmem_st_16(tmem + lane_off + c0, c);
+  }
+  // scale cells in the atom layout the GEMMs use: lane 32q + i, column k
+  // holds the four bytes of row i + 32 k (the same in every lane quarter)
+  uint4 wa, wb0, wb1;
+  const uint32_t* fa = reinterpret_cast<const uint32_t*>(sfA);
+  const uint32_t* fb = reinterpret_cast<const uint32_t*>(sfB);
+  wa = make_uint4(fa[lane], fa[lane + 32], fa[lane + 64], fa[lane + 96]);
+  wb0 = make_uint4(fb[lane], fb[lane + 32], fb[lane + 64], fb[lane + 96]);
+  wb1 = make_uint4(fb[128 + lane], fb[128 + lane + 32], fb[128 + lane + 64], fb[128 + lane + 96]);
+  tmem_st_4(tmem + lane_off + kXScaleA, wa);
+  tmem_st_4(tmem + lane_off + kXScaleB, wb0);
+  tmem_st_4(tmem + lane_off + kXScaleB + 4, wb1);
+  tc_wait_st();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0) {
+    const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sa)), bd = sdesc_kmajor_sw128(smem_u32(sb));
+    if (kind == 0)
+      mma_mxf8(tmem, ad, bd, idesc, tmem + kXScaleA, tmem + kXScaleB, 1u);
+    else if (kind == 1)
+      mma_mxf4(tmem, ad, bd, idesc, tmem + kXScaleA, tmem + kXScaleB, 1u);
+    else
+      mma_nvf4(tmem, ad, bd, idesc, tmem + kXScaleA, tmem + kXScaleB, 1u);
+    tc_commit(smem_u32(&bar));
+  }
+  if (!mbar_wait(smem_u32(&bar), 0)) atomicOr(&g_probe_error, kErrTimeout);
+  tc_fence_after();
+  for (int c0 = 0; c0 < XN; c0 += 16) {
+    uint32_t d[16];
+    tmem_ld_16(tmem + lane_off + c0, d);
+    tc_wait_ld_16(d);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) D[row * XN + c0 + j] = __uint_as_float(d[j]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_mma_probe_mx(int kind, const uint8_t* A, const uint8_t* sfA, const uint8_t* B,
+                                const uint8_t* sfB, const float* C, float* D, int afmt, int bfmt,
+                                cudaStream_t s) {
+  uint32_t idesc;
+  if (kind == 0)
+    idesc = idesc_mxf8(static_cast<uint32_t>(afmt), static_cast<uint32_t>(bfmt), PM, XN, 0u, 0u);
+  else if (kind == 1)
+    idesc = idesc_mxf4(PM, XN, 0u, 0u);
+  else
+    idesc = idesc_nvf4(PM, XN);
+  const size_t smem = (PM + XN) * 128 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(mma_probe_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  mma_probe_mx_kernel<<<1, 128, smem, s>>>(A, sfA, B, sfB, C, D, kind, idesc);
+  return cudaGetLastError();
+}
 
 cudaError_t mma_probe_error_read_and_clear(cudaStream_t s, uint32_t* out) {
   uint32_t zero = 0;

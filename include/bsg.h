@@ -386,6 +386,34 @@ bsg_status bsg_mma_peak(bsg_format fmt, int block_scaled, int pair, int64_t iter
  *         tensor memory before the MMA).
  * Errors: BSG_ERR_INVALID_ARG (null), BSG_ERR_UNSUPPORTED (non-FP8 format),
  *         BSG_ERR_ALIGNMENT, BSG_ERR_CUDA. */
+/* bsg_mma_probe_mx - one block-scaled tensor-core MMA on given operands and
+ * scales (verification only).
+ *
+ * The block-scaled counterpart of bsg_mma_probe: "Exact models of AMD matrix
+ * cores", section 3, fits a matrix unit's arithmetic with test vectors and
+ * random campaigns, and "FP8 MMA internals on Hopper" gives the fused
+ * dot-add structure such a fit starts from.  Runs exactly one
+ *     D[128][256] = sum_k (sA_r a_rk)(sB_c b_ck) + C[128][256]
+ * MMA of the shape and tensor-memory scale layout bsg_gemm's block-scaled
+ * kernels use, on one CTA:
+ *   kind 0  kind::mxf8f6f4.block_scale.scale_vec::1X: K = 32 FP8 values per
+ *           row (formats fa, fb: BSG_E4M3 / BSG_E5M2), scale byte 0 of the
+ *           row's cell (UE8M0);
+ *   kind 1  kind::mxf4.block_scale.scale_vec::2X: K = 64 packed E2M1 values,
+ *           bytes 0 and 1 (UE8M0) for elements 0-31 and 32-63;
+ *   kind 2  kind::mxf4nvf4.block_scale.scale_vec::4X: K = 64 packed E2M1,
+ *           bytes 0-3 (UE4M3) for each 16 elements.
+ * A    device, [128][32] bytes: row r's operand bytes in K order (FP8 one per
+ *      byte; E2M1 two per byte, first in the low nibble).
+ * sfA  device, [128][4] bytes: row r's scale cell.
+ * B    device, [256][32] bytes (column c of D = row c of B); sfB [256][4].
+ * C    device, [128][256] FP32 accumulator in; D device, [128][256] FP32 out.
+ * Errors: BSG_ERR_INVALID_ARG (null, kind not 0-2), BSG_ERR_UNSUPPORTED
+ *         (kind 0 with non-FP8 formats), BSG_ERR_CUDA. */
+bsg_status bsg_mma_probe_mx(int kind, const uint8_t* A, const uint8_t* sfA, const uint8_t* B,
+                           const uint8_t* sfB, const float* C, float* D, bsg_format fa,
+                           bsg_format fb, void* stream);
+
 bsg_status bsg_mma_probe(const uint8_t* A, bsg_format fa, const uint8_t* B, bsg_format fb,
                          const float* C, float* D, void* stream);
 

@@ -299,3 +299,49 @@ def test_nvfp4_closed_form_with_mixed_block_scales():
     sfB = np.full((N, K // 16), 0x38, np.uint8)
     D, _ = gemm.gemm_nvfp4(A, sfA, B, sfB, alpha=3.0)
     assert np.all(D == 3.0 * (16 * 2.0 + 48 * 0.5))
+
+
+def _pow2_scales(rng, rows, blocks, lo, hi):
+    return (127 + rng.integers(lo, hi + 1, (rows, blocks))).astype(np.uint8)
+
+
+def test_mx_bits_emulation_equals_exact_gemm_when_nothing_rounds():
+    # Operands whose partial sums all fit FP32's 24 bits and lie inside every
+    # alignment window: the MMA chain must then return the exact GEMM of
+    # gemm_mxfp8 / gemm_mxfp4 / gemm_nvfp4 (pinned above), so a wrong scale
+    # index, block, operand or K order in the emulation shows up here.
+    rng = np.random.default_rng(21)
+    M, N = 6, 5
+    i, j = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    i, j = i.ravel(), j.ravel()
+    # MXFP8: E4M3 normals in [1, 8) (codes 0x38..0x4F, both signs), scales 2^0..2^1
+    K = 96
+    codes = np.r_[np.arange(0x38, 0x50), np.arange(0xB8, 0xD0)].astype(np.uint8)
+    A, B = rng.choice(codes, (M, K)), rng.choice(codes, (N, K))
+    sA, sB = _pow2_scales(rng, M, K // 32, 0, 1), _pow2_scales(rng, N, K // 32, 0, 1)
+    C = rng.integers(-64, 64, (M, N)).astype(np.float32)
+    Dx, _ = gemm.gemm_mxfp8(A, "e4m3", sA, B, "e4m3", sB, C=C)
+    E = gemm.gemm_mx_bits("mxfp8", A, sA, B, sB, i, j, "e4m3", "e4m3", C=C)
+    assert np.array_equal(E, Dx[i, j])
+    # MXFP4: all E2M1 codes, scales 2^-2..2^2, K = 160 (a half-filled tail MMA)
+    K = 160
+    pa = formats.pack_e2m1(rng.integers(0, 16, (M, K)).astype(np.uint8))
+    pb = formats.pack_e2m1(rng.integers(0, 16, (N, K)).astype(np.uint8))
+    sA, sB = _pow2_scales(rng, M, K // 32, -2, 2), _pow2_scales(rng, N, K // 32, -2, 2)
+    Dx, _ = gemm.gemm_mxfp4(pa, sA, pb, sB)
+    E = gemm.gemm_mx_bits("mxfp4", pa, sA, pb, sB, i, j)
+    assert np.array_equal(E, Dx[i, j])
+    # NVFP4: E2M1 codes of magnitude <= 2, E4M3 scales 0.5..3.75, alpha = 2^-3
+    K = 128
+    small = np.r_[0:5, 8:13].astype(np.uint8)
+    pa = formats.pack_e2m1(rng.choice(small, (M, K)))
+    pb = formats.pack_e2m1(rng.choice(small, (N, K)))
+    sA = rng.integers(0x30, 0x48, (M, K // 16)).astype(np.uint8)
+    sB = rng.integers(0x30, 0x48, (N, K // 16)).astype(np.uint8)
+    C = rng.integers(-64, 64, (M, N)).astype(np.float32)
+    Dx, _ = gemm.gemm_nvfp4(pa, sA, pb, sB, alpha=0.125, C=C)
+    E = gemm.gemm_mx_bits("nvfp4", pa, sA, pb, sB, i, j, C=C, alpha=0.125)
+    assert np.array_equal(E, Dx[i, j])
+    # BF16 output is the round-to-nearest-even of the FP32 result
+    Eb = gemm.gemm_mx_bits("nvfp4", pa, sA, pb, sB, i, j, C=C, alpha=0.125, out="bf16")
+    assert np.array_equal(Eb, gemm.bf16_round(Dx[i, j]))
