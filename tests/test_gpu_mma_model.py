@@ -33,7 +33,7 @@ def _model(A, fa, B, fb, C):
     a = formats.decode_array(A, fa)
     b = formats.decode_array(B, fb)
     i, j = np.meshgrid(np.arange(128), np.arange(16), indexing="ij")
-    return fda.fda_batch(a[i.ravel()], b[j.ravel()], C.astype(np.float64).ravel()).reshape(128, 16)
+    return fda.fda_batch(a[i.ravel()], b[j.ravel()], C.astype(np.float64).ravel(), fa, fb).reshape(128, 16)
 
 
 @pytest.mark.parametrize("fa,fb", [("e4m3", "e4m3"), ("e5m2", "e4m3"), ("e4m3", "e5m2"), ("e5m2", "e5m2")])
