@@ -7,6 +7,8 @@
 #pragma once
 #include <cstdint>
 
+#include "common.cuh"
+
 namespace bsg {
 
 // Four FP32 values -> four FP8 codes, first value in the lowest byte.
@@ -69,12 +71,20 @@ __device__ __forceinline__ uint32_t fp8_codes4(int fmt, const GroupDiv& d, float
                                                float e) {
   float q[4] = {a, b, c, e};
   if (d.fast) {
+    // the same steps on pairs (fma.rn.f32x2 rounds each half like fmaf):
+    // t = x r; t = (x - t s) r + t, twice; -t s + x is written t (-s) + x
+    const uint64_t r2 = f32x2_pack(d.r, d.r), ns2 = f32x2_pack(-d.s, -d.s);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float x = q[i];
-      float t = x * d.r;
-      t = fmaf(fmaf(-t, d.s, x), d.r, t);
-      q[i] = fmaf(fmaf(-t, d.s, x), d.r, t);
+    for (int i = 0; i < 4; i += 2) {
+      const uint64_t x2 = f32x2_pack(q[i], q[i + 1]);
+      uint64_t t = fmul2(x2, r2);
+      uint64_t rem = x2;
+      ffma2(rem, t, ns2);
+      ffma2(t, rem, r2);
+      rem = x2;
+      ffma2(rem, t, ns2);
+      ffma2(t, rem, r2);
+      f32x2_unpack(t, q[i], q[i + 1]);
     }
   } else {
 #pragma unroll

@@ -133,12 +133,49 @@ __global__ void __launch_bounds__(kTileThreads) quantize_fp8_tile_kernel(
   }
 }
 
-// Block (8 rows) x (4 K tiles of 128): warp w takes row 8*blockIdx.x + w and
-// K tiles 4*blockIdx.y .. +3, lane l columns 4l..4l+3 of each.  Scales are
-// stored K-tile major, scales[t * rows + row], so a block's eight rows of one
-// K tile fill one 32-byte sector.
+// Row quantiser (1 x 128 groups along each row).  A warp takes 512-column
+// chunks of rows, lane l the 16 consecutive values 16l..16l+15, so the eight
+// lanes of a 128-wide group find its maximum in three shuffle levels, and
+// every lane loads and stores whole 16-byte pieces.  The warps walk the
+// chunks grid-stride, each loading its next chunk before it converts the
+// current one, so two chunks' loads are in flight per warp.  Scales are
+// stored K-tile major, scales[t * rows + row], as the GEMM reads them.
 constexpr int kRowWarps = 8;
-constexpr int kRowTiles = 4;
+
+template <bool kBF16>
+__device__ __forceinline__ void load16(const void* x, int64_t row, int64_t col, int64_t cols, int64_t ld,
+                                       bool vec_ok, float (&v)[16]) {
+  if (kBF16) {
+    const uint16_t* p = static_cast<const uint16_t*>(x) + row * ld + col;
+    if (vec_ok && col + 15 < cols) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + h);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[8 * h + 2 * j] = __uint_as_float(w[j] << 16);
+          v[8 * h + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = (col + j < cols) ? bf16_to_f32(p[j]) : 0.0f;
+    }
+  } else {
+    const float* p = static_cast<const float*>(x) + row * ld + col;
+    if (vec_ok && col + 15 < cols) {
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const float4 u = __ldg(reinterpret_cast<const float4*>(p) + h);
+        v[4 * h] = u.x; v[4 * h + 1] = u.y; v[4 * h + 2] = u.z; v[4 * h + 3] = u.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = (col + j < cols) ? p[j] : 0.0f;
+    }
+  }
+}
 
 template <bool kBF16>
 __global__ void __launch_bounds__(kRowWarps * 32) quantize_fp8_row_kernel(
@@ -146,50 +183,60 @@ __global__ void __launch_bounds__(kRowWarps * 32) quantize_fp8_row_kernel(
     bool vec_in, bool vec_out, uint8_t* __restrict__ q, float* __restrict__ scales) {
   grid_dep_launch();
   grid_dep_wait();
-  const int64_t kt = (cols + 127) / 128;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
-  const int64_t t0 = static_cast<int64_t>(blockIdx.y) * kRowTiles;
   const int lane = threadIdx.x & 31;
-  if (row >= rows) return;   // uniform across the warp
-  float v[kRowTiles][4];
-#pragma unroll
-  for (int i = 0; i < kRowTiles; ++i) {
-    const int64_t col = (t0 + i) * 128 + 4 * lane;
-    if (t0 + i < kt && col < cols) {
-      load4<kBF16>(x, row, col, cols, ld, vec_in, v[i]);
+  const int64_t chunks = (cols + 511) / 512;    // 512-column chunks per row
+  const int64_t total = rows * chunks;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kRowWarps;
+  // chunk w's row and this lane's first column in it
+  auto where = [&](int64_t w, int64_t& row, int64_t& col) {
+    row = w / chunks;
+    col = (w - row * chunks) * 512 + 16 * lane;
+  };
+  auto load = [&](int64_t w, float (&v)[16]) {
+    int64_t row, col;
+    where(w, row, col);
+    if (w < total && col < cols) {
+      load16<kBF16>(x, row, col, cols, ld, vec_in, v);
     } else {
-      v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = 0.0f;   // past the row's end: no effect on the maximum
     }
-  }
-  // group maxima (every lane ends with all four), then lane i computes the
-  // scale and its reciprocal of group i - the correctly rounded divisions
-  // run once per group instead of once per lane - and broadcasts them
-  float am[kRowTiles];
+  };
+  auto convert = [&](int64_t w, const float (&v)[16]) {
+    int64_t row, col;
+    where(w, row, col);
+    float a = 0.0f;
 #pragma unroll
-  for (int i = 0; i < kRowTiles; ++i) {
-    float a = fmaxf(fmaxf(fabsf(v[i][0]), fabsf(v[i][1])), fmaxf(fabsf(v[i][2]), fabsf(v[i][3])));
+    for (int j = 0; j < 16; ++j) a = fmaxf(a, fabsf(v[j]));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    am[i] = a;
-  }
-  float mine = am[0];
+    for (int o = 4; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const float sc = fp8_scale(a, fmt_max);
+    const GroupDiv div(sc, __frcp_rn(sc));
+    uint32_t c[4];
 #pragma unroll
-  for (int i = 1; i < kRowTiles; ++i) mine = lane == i ? am[i] : mine;
-  const float my_s = fp8_scale(mine, fmt_max);
-  const float my_r = __frcp_rn(my_s);
-#pragma unroll
-  for (int i = 0; i < kRowTiles; ++i) {
-    const int64_t t = t0 + i;
-    if (t >= kt) break;  // uniform across the warp
-    const float s = __shfl_sync(0xffffffffu, my_s, i);
-    const float r = __shfl_sync(0xffffffffu, my_r, i);
-    const int64_t col = t * 128 + 4 * lane;
-    if (lane == 0) scales[t * rows + row] = s;
+    for (int i = 0; i < 4; ++i) c[i] = fp8_codes4(fmt, div, v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     if (col < cols) {
-      const GroupDiv div(s, r);
-      const uint32_t c = fp8_codes4(fmt, div, v[i][0], v[i][1], v[i][2], v[i][3]);
-      store_codes4(q, row * cols + col, col, cols, vec_out, c);
+      uint8_t* dst = q + row * cols + col;
+      if (vec_out && col + 15 < cols) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(c[0], c[1], c[2], c[3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (col + j < cols) dst[j] = static_cast<uint8_t>(c[j / 4] >> (8 * (j % 4)));
+      }
+      if ((lane & 7) == 0) scales[(col / 128) * rows + row] = sc;   // the group's first lane
     }
+  };
+  // w is uniform across the warp, so are the loop's branches
+  int64_t w = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
+  float va[16], vb[16];
+  load(w, va);
+  for (; w < total; w += 2 * stride) {
+    load(w + stride, vb);
+    convert(w, va);
+    if (w + stride >= total) break;
+    load(w + 2 * stride, va);
+    convert(w + stride, vb);
   }
 }
 
@@ -411,11 +458,19 @@ cudaError_t launch_quantize_fp8_tile(const void* x, bool src_bf16, int64_t rows,
 cudaError_t launch_quantize_fp8_row(const void* x, bool src_bf16, int64_t rows, int64_t cols,
                                     int64_t ld, int fmt, float fmt_max, uint8_t* q, float* scales,
                                     cudaStream_t s) {
-  const bool vec_in = src_bf16 ? (aligned(x, 8) && ld % 4 == 0) : (aligned(x, 16) && ld % 4 == 0);
-  const bool vec_out = aligned(q, 4) && cols % 4 == 0;
-  const int64_t kt = (cols + 127) / 128;
-  const dim3 grid(static_cast<unsigned>((rows + kRowWarps - 1) / kRowWarps),
-                  static_cast<unsigned>((kt + kRowTiles - 1) / kRowTiles));
+  // 16-byte loads of a lane's 16 values (FP32: four, BF16: two) and one
+  // 16-byte store of its codes, where alignment allows
+  const bool vec_in = aligned(x, 16) && ld % (src_bf16 ? 8 : 4) == 0;
+  const bool vec_out = aligned(q, 16) && cols % 16 == 0;
+  // enough warps to fill the GPU once; each walks several chunks
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 1;
+  const int64_t warps = rows * ((cols + 511) / 512);
+  int64_t blocks = (warps + kRowWarps - 1) / kRowWarps;
+  if (blocks > static_cast<int64_t>(sms) * 4) blocks = static_cast<int64_t>(sms) * 4;
+  const dim3 grid(static_cast<unsigned>(blocks));
   auto kern = src_bf16 ? quantize_fp8_row_kernel<true> : quantize_fp8_row_kernel<false>;
   return launch_pdl(kern, grid, dim3(kRowWarps * 32), 0, s, x, rows, cols, ld, fmt, fmt_max,
                     vec_in, vec_out, q, scales);
