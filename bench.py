@@ -146,6 +146,12 @@ class Workload:
         self.q8out = name == "ffn_up_q8out"
         self.nv4 = name == "nvfp4_ffn_up"
         self.bs16 = name == "bs16_ffn_up"
+        # decode: the BF16 activations are quantised on the fly inside one
+        # API call (bsg_gemm_mxfp4_act); up to four rows in the GEMM kernel
+        # itself, above that by the quantiser launched first
+        self.act = name == "decode"
+        self.act_fused = self.act and M <= 4
+        self.launches_per_step = 1 if self.act_fused else 2
         self.g_a, self.g_b = 1.0, 2.0 ** -6      # NVFP4 tensor scales
         if name == "ffn_up":
             self.fa, self.fb, self.ga, self.gb, self.out = "e4m3", "e4m3", "row", "tile", "bf16"
@@ -216,6 +222,9 @@ class Workload:
         self.D_host = torch.empty_like(self.D, device="cpu").pin_memory()
         self.sD_host = torch.empty_like(self.sets[0]["sD"], device="cpu").pin_memory() if self.q8out else None
         self.ws = bsg.workspace_for(M, N, K, self.fa, self.fb, dev)
+        if self.act:
+            n = max(bsg.bsg_gemm_mxfp4_act_workspace_size(M, N, K), 16)
+            self.ws_act = torch.zeros((n,), dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
 
     def quantize(self, r=0):
@@ -231,8 +240,16 @@ class Workload:
         else:
             b.bsg_quantize_fp8(st["A"], self.fa, self.ga, q=st["qa"], scales=st["sa"])
 
+    def act_gemm(self, r=0):
+        st = self.sets[r]
+        self.bsg.bsg_gemm_mxfp4_act(st["A"], st["qb"], st["sb"], out=self.out, D=st["D"],
+                                    workspace=self.ws_act)
+
     def gemm(self, r=0):
         st = self.sets[r]
+        if self.act_fused:        # the dominant kernel is the fused call itself
+            self.act_gemm(r)
+            return
         if self.nv4:
             self.bsg.bsg_gemm_nvfp4(st["qa"], st["sa"], st["qb"], st["sb"], alpha=self.g_a * self.g_b,
                                     out=self.out, D=st["D"], K=self.K)
@@ -245,10 +262,11 @@ class Workload:
                           out=self.out, D=st["D"], workspace=self.ws, K=self.K)
 
     def step(self, r=0):
+        if self.act:
+            self.act_gemm(r)
+            return
         self.quantize(r)
         self.gemm(r)
-
-    launches_per_step = 2
 
     # algorithmic quantities
     def flops(self):
@@ -264,7 +282,8 @@ class Workload:
             a = M * K / 2 + M * K / 32 * 2
             b = N * K / 2 + N * K / 32 * 2
         elif self.fp4:
-            a = M * K / 2 + M * K / 32
+            # fused decode: the kernel reads the BF16 activations themselves
+            a = M * K * 2 if self.act_fused else M * K / 2 + M * K / 32
             b = N * K / 2 + N * K / 32
         elif self.mx8:
             a = M * K + M * K / 32
@@ -280,6 +299,8 @@ class Workload:
 
     def step_bytes(self):
         """Algorithmic bytes of a whole step (quantiser read + write, GEMM)."""
+        if self.act_fused:
+            return self.gemm_bytes()          # the activations are read once, by the GEMM
         src = self.M * self.K * (2 if self.name == "decode" else 4)
         return src + self.gemm_bytes()
 

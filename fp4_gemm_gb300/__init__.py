@@ -34,7 +34,8 @@ EXPORTS = ("bsg_quantize_fp8", "bsg_quantize_mxfp4", "bsg_gemm", "bsg_gemm_works
            "bsg_scale_bytes", "bsg_sf_to_tcgen05", "bsg_status_string", "bsg_device_error",
            "bsg_num_sms", "bsg_gemm_decode_noalloc", "bsg_mma_peak", "bsg_quantize_mx",
            "bsg_mma_probe", "bsg_gemm_quantized", "bsg_quantize_nvfp4", "bsg_gemm_nvfp4",
-           "bsg_check_wait_timeout", "bsg_quantize_fp4_bs16", "bsg_mma_probe_mx")
+           "bsg_check_wait_timeout", "bsg_quantize_fp4_bs16", "bsg_mma_probe_mx",
+           "bsg_gemm_mxfp4_act", "bsg_gemm_mxfp4_act_workspace_size")
 
 
 class BsgError(RuntimeError):
@@ -68,6 +69,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsg_gemm_quantized.restype = i32
     lib.bsg_gemm_workspace_size.argtypes = [i64, i64, i64, i32, i32]
     lib.bsg_gemm_workspace_size.restype = sz
+    lib.bsg_gemm_mxfp4_act.argtypes = [i64, i64, i64, vp, i32, i64, vp, vp, vp, vp, i32, vp, sz, vp]
+    lib.bsg_gemm_mxfp4_act.restype = i32
+    lib.bsg_gemm_mxfp4_act_workspace_size.argtypes = [i64, i64, i64]
+    lib.bsg_gemm_mxfp4_act_workspace_size.restype = sz
     lib.bsg_scale_bytes.argtypes = [i64, i64, i32, i32]
     lib.bsg_scale_bytes.restype = sz
     lib.bsg_sf_to_tcgen05.argtypes = [vp, i64, i64, vp, vp]
@@ -390,6 +395,46 @@ def bsg_gemm(A: torch.Tensor, fa: str, sA: torch.Tensor, ga: str,
                         _ptr(sB), GRAN[gb], _ptr(C), _ptr(D), DTYPE[out], _ptr(workspace),
                         0 if workspace is None else workspace.numel(), _stream(stream)),
            "bsg_gemm")
+    return D
+
+
+_act_workspaces: dict = {}
+
+
+def bsg_gemm_mxfp4_act_workspace_size(M: int, N: int, K: int) -> int:
+    return int(load_library().bsg_gemm_mxfp4_act_workspace_size(M, N, K))
+
+
+def bsg_gemm_mxfp4_act(x: torch.Tensor, B: torch.Tensor, sB: torch.Tensor,
+                       C: torch.Tensor | None = None, out: str = "bf16", D: torch.Tensor | None = None,
+                       workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """D = sum_k (s_A a_k)(s_B b_k) + C with the activations x (M, K; FP32 or
+    BF16, rows may be padded) quantised to MXFP4 inside the call, exactly as
+    bsg_quantize_mxfp4 would.  B: (N, K/2) packed E2M1, sB: tcgen05-layout
+    E8M0 scales.  The workspace (zero-filled once) is cached per device and
+    problem shape: after a call only its counters and partial sums are zero,
+    its activation area is scratch, so another shape gets its own."""
+    lib = load_library()
+    M, K = x.shape
+    N = B.shape[0]
+    if x.dtype not in (torch.float32, torch.bfloat16) or x.stride(1) != 1:
+        raise ValueError("x must be FP32 or BF16 with unit column stride")
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.float32 if out == "f32" else torch.bfloat16, device=x.device)
+    if workspace is None:
+        n = max(bsg_gemm_mxfp4_act_workspace_size(M, N, K), 16)
+        dev = torch.device(x.device)
+        key = (dev.type, dev.index, M, N, K)
+        ws = _act_workspaces.get(key)
+        if ws is None or ws.numel() < n:
+            ws = torch.zeros((n,), dtype=torch.uint8, device=dev)
+            _act_workspaces[key] = ws
+        workspace = ws
+    _need_cuda(x, B, sB, C, D, workspace)
+    _check(lib.bsg_gemm_mxfp4_act(M, N, K, _ptr(x), DTYPE["bf16" if x.dtype == torch.bfloat16 else "f32"],
+                                  x.stride(0), _ptr(B), _ptr(sB), _ptr(C), _ptr(D), DTYPE[out],
+                                  _ptr(workspace), workspace.numel(), _stream(stream)),
+           "bsg_gemm_mxfp4_act")
     return D
 
 

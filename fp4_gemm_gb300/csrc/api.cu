@@ -299,6 +299,61 @@ size_t bsg_gemm_workspace_size(int64_t M, int64_t N, int64_t K, bsg_format fa, b
 }
 
 
+size_t bsg_gemm_mxfp4_act_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || K % 32) return 0;
+  const int sms = num_sms_current();
+  return bsg::gemm_mxfp4_act_workspace(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                                       sms > 0 ? sms : 1, nullptr);
+}
+
+bsg_status bsg_gemm_mxfp4_act(int64_t M, int64_t N, int64_t K, const void* x, bsg_dtype src,
+                              int64_t ldx, const void* B, const void* sB, const float* C, void* D,
+                              bsg_dtype out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (x == nullptr || B == nullptr || sB == nullptr || D == nullptr) return BSG_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || K % 32 || ldx < K)
+    return BSG_ERR_INVALID_ARG;
+  if (src != BSG_F32 && src != BSG_BF16) return BSG_ERR_INVALID_ARG;
+  if (out != BSG_F32 && out != BSG_BF16) return BSG_ERR_INVALID_ARG;
+  if (!aligned(x, src == BSG_F32 ? 4 : 2) || !aligned(B, 16) || !aligned(sB, 16) ||
+      !aligned(D, out == BSG_F32 ? 4 : 2) || (C != nullptr && !aligned(C, 4)))
+    return BSG_ERR_ALIGNMENT;
+  const int sms = num_sms_current();
+  if (sms <= 0) return BSG_ERR_CUDA;
+  size_t off[3];
+  const size_t need = bsg::gemm_mxfp4_act_workspace(static_cast<int>(M), static_cast<int>(N),
+                                                    static_cast<int>(K), sms, off);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)))
+    return BSG_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M > bsg::kActFusedMaxM) {
+    // the stand-alone quantiser into the workspace, then the GEMM (with the
+    // decode kernel's split-K area at the front of the workspace)
+    uint8_t* xq = ws + off[1];
+    uint8_t* xsf = ws + off[2];
+    const bsg_status st = bsg_quantize_mxfp4(x, src, M, K, ldx, xq, xsf, BSG_SF_TCGEN05, stream);
+    if (st != BSG_OK) return st;
+    return bsg_gemm(M, N, K, xq, BSG_E2M1, xsf, BSG_SCALE_BLOCK1x32_E8M0, B, BSG_E2M1, sB,
+                    BSG_SCALE_BLOCK1x32_E8M0, C, D, out, off[1] > 0 ? workspace : nullptr, off[1], stream);
+  }
+  Mxfp4GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.sfB = static_cast<const uint8_t*>(sB);
+  a.C = C;
+  a.D = D;
+  a.out_bf16 = out == BSG_BF16;
+  a.workspace = need > 0 ? workspace : nullptr;   // the split-K area, when the plan has one
+  a.workspace_bytes = need;
+  a.B = B;
+  a.xsrc = x;
+  a.ldx = ldx;
+  a.xsrc_bf16 = src == BSG_BF16;
+  return from_cuda(bsg::launch_gemm_mxfp4_decode(a, sms, s));
+}
+
 bsg_status bsg_gemm_quantized(int64_t M, int64_t N, int64_t K, const void* A, bsg_format fa,
                               const void* sA, bsg_scale_gran ga, const void* B, bsg_format fb,
                               const void* sB, bsg_scale_gran gb, const float* C, bsg_format qfmt,

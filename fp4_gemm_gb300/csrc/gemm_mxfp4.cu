@@ -33,8 +33,11 @@
 //    a CTA whose range covers only part of a tile's K writes an FP32 partial
 //    to the workspace, and the last contributor (per-tile counter) adds the
 //    partials in a fixed order, so results are deterministic.
+#include <cstring>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "quant_math.cuh"
 
 namespace bsg {
 namespace {
@@ -366,6 +369,10 @@ struct __align__(1024) Smem {
   uint64_t tfull[2];     // accumulator buffer holds a finished segment
   uint64_t tempty[2];    // epilogue drained the buffer
   uint64_t final_bar;
+  // on-the-fly activations: per stage (two in turn) and 4-block atom, each
+  // activation row's four E8M0 codes, the first word of its scale cell
+  uint32_t xsc[2][2 * CH][32];
+  uint64_t xbar[2];      // all 128 scale-writer threads wrote stage buffer b's codes
   uint32_t tmem_base;
   uint32_t fast_flag;
   uint32_t last_flag;
@@ -410,6 +417,83 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   return v;
 }
 
+// One 32-value block of activation row r quantised to MXFP4 with the rule of
+// the stand-alone quantiser ("Rubin FP4 GEMM deep dive" section 4.2): the
+// E8M0 code of the power of two nearest max|x| / 6, then E2M1(x * 2^-e),
+// two codes per byte, first value in the low nibble.  Returns the code.
+__device__ __forceinline__ uint32_t quantize_block_mxfp4(const void* x, bool bf16, bool vec, int64_t ldx,
+                                                         int r, int64_t b, uint4& codes) {
+  float v[32];
+  if (bf16) {
+    const uint16_t* p = static_cast<const uint16_t*>(x) + r * ldx + b * 32;
+    if (vec) {
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + h);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[8 * h + 2 * j] = __uint_as_float(w[j] << 16);
+          v[8 * h + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(static_cast<uint32_t>(p[j]) << 16);
+    }
+  } else {
+    const float* p = static_cast<const float*>(x) + r * ldx + b * 32;
+    if (vec) {
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const float4 u = __ldg(reinterpret_cast<const float4*>(p) + h);
+        v[4 * h] = u.x; v[4 * h + 1] = u.y; v[4 * h + 2] = u.z; v[4 * h + 3] = u.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = p[j];
+    }
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  // The E8M0 code of the power of two nearest RN(amax / 6), without the
+  // division: with amax = m 2^e (1 <= m < 2), amax / 6 = (m / 1.5) 2^(e-2),
+  // which is 2^(e-2) after that rounding when m >= 1.125 and 2^(e-3) below.
+  // RN to FP32 cannot move the quotient across the boundary: m / 0.75 is
+  // 1.5 only at m = 1.125 exactly (a tie, rounded up like the rule does) and
+  // never reaches 2.  Zero, tiny (quotient near the subnormals), infinite or
+  // NaN maxima take the rule itself.
+  const uint32_t ab = __float_as_uint(amax);
+  const int ef = static_cast<int>(ab >> 23);          // amax >= 0: no sign bit
+  const uint32_t code = (ef < 27 || ef == 255)
+                            ? e8m0_nearest(__fdiv_rn(amax, 6.0f))
+                            : static_cast<uint32_t>(ef - 2 - ((ab & 0x7FFFFFu) >= 0x100000u ? 0 : 1));
+  // 2^-(code-127) as an FP32 normal: code in [0,254] -> exponent field 254-code
+  const float inv = __uint_as_float(static_cast<uint32_t>(254 - static_cast<int>(code)) << 23);
+  const uint64_t inv2 = f32x2_pack(inv, inv);
+  uint32_t w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    w[q] = 0u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float lo, hi;
+      f32x2_unpack(fmul2(f32x2_pack(v[8 * q + 2 * j], v[8 * q + 2 * j + 1]), inv2), lo, hi);
+      w[q] |= cvt2_e2m1(lo, hi) << (8 * j);
+    }
+  }
+  codes = make_uint4(w[0], w[1], w[2], w[3]);
+  return code;
+}
+
+// Byte offset of the 16-byte piece p (0..7) of row r in a K-major tile with
+// 128-byte rows in the 128-byte swizzle (the layout a SWIZZLE_128B TMA box
+// writes): 8-row atoms of 1024 bytes, piece index XOR the row within its atom.
+__device__ __forceinline__ uint32_t swz128_piece(int r, int p) {
+  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + (((p ^ r) & 7) << 4));
+}
+
 template <int NX, bool kBF16Out>
 __device__ __forceinline__ void store_row(const float (&v)[NX], const float* __restrict__ Cin,
                                           void* __restrict__ Dout, int M, int N, int64_t n) {
@@ -427,14 +511,23 @@ __device__ __forceinline__ void store_row(const float (&v)[NX], const float* __r
   }
 }
 
-template <int NX, int CH, bool kBF16Out>
+// kQ: the activations arrive unquantised (FP32 or BF16, xsrc with row pitch
+// ldx; qflags bit 0: BF16, bit 1: 16-byte loads allowed) and are quantised
+// stage by stage by the scale-writer warps: each stage's K slice of all
+// activation rows goes to MXFP4 codes written straight into the stage's
+// shared-memory operand, in the 128-byte swizzle a TMA load would produce,
+// and E8M0 codes stored into the tensor-memory scale cells - so the TMA
+// moves weights only, and no other kernel or CTA is waited for.  tmX and sfX
+// are not used then.
+template <int NX, int CH, bool kBF16Out, bool kQ>
 __global__ void __launch_bounds__(kDecThreads, 1)
     gemm_mxfp4_decode_kernel(const __grid_constant__ CUtensorMap tmX,
                              const __grid_constant__ CUtensorMap tmW,
                              const uint8_t* __restrict__ sfX, const uint8_t* __restrict__ sfW,
                              const float* __restrict__ Cin, void* __restrict__ Dout, int M, int N,
                              int K, int64_t KS, int64_t U, int64_t smax,
-                             float* __restrict__ ws, uint32_t* __restrict__ counters) {
+                             float* __restrict__ ws, uint32_t* __restrict__ counters,
+                             const void* __restrict__ xsrc, int64_t ldx, int qflags) {
   constexpr int kStages = Cfg<NX, CH>::kStages;
   constexpr int kSfCols = Cfg<NX, CH>::kSfColsPerStage;
   constexpr int kSfBase = Cfg<NX, CH>::kSfBase;
@@ -459,6 +552,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&sm.tfull[b]), 1);
       mbar_init(smem_u32(&sm.tempty[b]), 4);
+      mbar_init(smem_u32(&sm.xbar[b]), 128);
     }
     mbar_init(smem_u32(&sm.final_bar), 1);
     sm.abort_flag = 0u;
@@ -485,7 +579,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const uint64_t keep = l2_policy_evict_last();    // activations: re-read by every CTA
       const uint64_t stream = l2_policy_evict_first(); // weights: read exactly once
       uint32_t it = 0;
-      for (int64_t u = u0; u < u1; ++u, ++it) {
+      int64_t u = u0;
+      for (; u < u1; ++u, ++it) {
         const int s = static_cast<int>(it % kStages);
         const uint32_t ph = (it / kStages) & 1u;
         if (sm.abort_flag) break;
@@ -496,13 +591,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const int64_t tile = u / KS;
         const int c0 = static_cast<int>(u % KS) * CH;    // first 128-byte chunk
         const uint32_t fb = smem_u32(&sm.full[s]);
-        mbar_arrive_expect_tx(fb, CH * (128 + NX) * kRowBytes);
+        // kQ: the activation half of the stage is written by the scale writers
+        mbar_arrive_expect_tx(fb, CH * (kQ ? 128 : 128 + NX) * kRowBytes);
         if (CH == 1) {
           tma_load_2d_hint(smem_u32(sm.w[s]), &tmW, fb, c0 * kRowBytes, static_cast<int32_t>(tile * 128), stream);
-          tma_load_2d_hint(smem_u32(sm.x[s]), &tmX, fb, c0 * kRowBytes, 0, keep);
+          if (!kQ) tma_load_2d_hint(smem_u32(sm.x[s]), &tmX, fb, c0 * kRowBytes, 0, keep);
         } else {
           tma_load_3d_hint(smem_u32(sm.w[s]), &tmW, fb, 0, static_cast<int32_t>(tile * 128), c0, stream);
-          tma_load_3d_hint(smem_u32(sm.x[s]), &tmX, fb, 0, 0, c0, keep);
+          if (!kQ) tma_load_3d_hint(smem_u32(sm.x[s]), &tmX, fb, 0, 0, c0, keep);
         }
       }
       drain_fills(sm.full, kStages, it);
@@ -602,11 +698,52 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const uint4* gx = reinterpret_cast<const uint4*>(sfX + static_cast<int64_t>(ka0) * kSfAtom) + lane;
       uint4 vw[2 * CH], vx[2 * CH];
 #pragma unroll
-      for (int a = 0; a < 2 * CH; ++a) {
-        if (a < na) {
-          vw[a] = __ldg(gw + a * (kSfAtom / 16));
-          vx[a] = __ldg(gx + a * (kSfAtom / 16));
+      for (int a = 0; a < 2 * CH; ++a)
+        if (a < na) vw[a] = __ldg(gw + a * (kSfAtom / 16));
+      if constexpr (kQ) {
+        // This stage's K slice (CH x 256 values) of every activation row,
+        // one 32-value block per item, items row-major so that neighbouring
+        // threads read neighbouring bytes.  Rows past M and blocks past K/32
+        // get zero codes and scale code 127, as a TMA load past the edge
+        // and the stand-alone quantiser's padding give.
+        constexpr int kBlocks = 8 * CH;                 // 32-value blocks in the slice
+        constexpr int kItems = NX * kBlocks / 128;      // per thread
+        static_assert(NX * kBlocks % 128 == 0, "whole items per thread");
+        const int t = static_cast<int>(threadIdx.x) - kSfWarp0 * 32;
+        const int64_t gb0 = static_cast<int64_t>(u % KS) * CH * 8;   // first block of the slice
+        const int buf = static_cast<int>(it & 1u);
+        uint8_t* xs = sm.x[s];
+#pragma unroll
+        for (int j = 0; j < kItems; ++j) {
+          const int i = t + 128 * j;
+          const int r = i / kBlocks, bb = i % kBlocks;
+          const int64_t gb = gb0 + bb;
+          uint4 codes = make_uint4(0u, 0u, 0u, 0u);
+          uint32_t code = 127u;
+          if (r < M && gb < K / 32)
+            code = quantize_block_mxfp4(xsrc, (qflags & 1) != 0, (qflags & 2) != 0, ldx, r, gb, codes);
+          st_shared_v4(smem_u32(xs + (bb >> 3) * NX * kRowBytes) + swz128_piece(r, bb & 7), codes);
+          reinterpret_cast<uint8_t*>(&sm.xsc[buf][bb >> 2][r])[bb & 3] = static_cast<uint8_t>(code);
         }
+        fence_proxy_async_smem();   // the codes are read by the tensor core (async proxy)
+        // all four scale-writer warps have written this stage's codes (a
+        // bounded wait: a warp that stopped on an abort cannot hang the rest);
+        // buffer it & 1 comes round again two stages later, after every
+        // thread has arrived on the stage in between, i.e. read this one
+        mbar_arrive(smem_u32(&sm.xbar[buf]));
+        if (!mbar_wait(smem_u32(&sm.xbar[buf]), (it >> 1) & 1u)) {
+          raise_abort(&sm.abort_flag);
+          break;
+        }
+#pragma unroll
+        for (int a = 0; a < 2 * CH; ++a)
+          if (a < na)
+            vx[a] = make_uint4(lane < NX ? sm.xsc[buf][a][lane] : 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu,
+                               0x7F7F7F7Fu);
+      } else {
+#pragma unroll
+        for (int a = 0; a < 2 * CH; ++a)
+          if (a < na) vx[a] = __ldg(gx + a * (kSfAtom / 16));
       }
       const uint32_t sfc = lane_base + kSfBase + s * kSfCols;
 #pragma unroll
@@ -796,27 +933,65 @@ size_t gemm_mxfp4_decode_workspace(int M, int N, int K, int num_sms) {
   return floats * sizeof(float) + static_cast<size_t>(p.tiles) * sizeof(uint32_t);
 }
 
+size_t gemm_mxfp4_act_workspace(int M, int N, int K, int num_sms, size_t* off) {
+  // The decode kernel's split-K area (M <= 32) first; unless the kernel
+  // quantises as it goes (M <= kActFusedMaxM), the activation codes and
+  // scale atoms follow, each at a 256-byte boundary.
+  auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+  const size_t split = M <= 32 ? gemm_mxfp4_decode_workspace(M, N, K, num_sms) : 0;
+  if (off != nullptr) off[0] = off[1] = off[2] = 0;
+  if (M <= kActFusedMaxM) return split;
+  const size_t codes = static_cast<size_t>(M) * (K / 2);
+  const size_t atoms = static_cast<size_t>((M + 127) / 128) * ((K / 32 + 3) / 4) * kSfAtom;
+  if (off != nullptr) {
+    off[1] = up(split);
+    off[2] = off[1] + up(codes);
+  }
+  return up(split) + up(codes) + atoms;
+}
+
 namespace {
-template <int NX, int CH, bool BF>
+template <int NX, int CH, bool BF, bool Q>
 cudaError_t launch_decode_variant(const Mxfp4GemmArgs& a, const decode::Plan& p, float* ws,
                                   uint32_t* counters, cudaStream_t s) {
   using namespace decode;
   CUtensorMap tmX, tmW;
+  std::memset(&tmX, 0, sizeof(tmX));   // not read when the activations come unquantised (Q)
   const uint64_t kb = static_cast<uint64_t>(a.K) / 2;
   if (CH == 1) {
-    if (!make_kmajor_map(&tmX, a.A, kb, a.M, kb, NX) || !make_kmajor_map(&tmW, a.B, kb, a.N, kb, 128))
+    if ((!Q && !make_kmajor_map(&tmX, a.A, kb, a.M, kb, NX)) || !make_kmajor_map(&tmW, a.B, kb, a.N, kb, 128))
       return cudaErrorInvalidValue;
   } else {
-    if (!make_kmajor_map_chunked(&tmX, a.A, kb, a.M, kb, NX, CH) ||
+    if ((!Q && !make_kmajor_map_chunked(&tmX, a.A, kb, a.M, kb, NX, CH)) ||
         !make_kmajor_map_chunked(&tmW, a.B, kb, a.N, kb, 128, CH))
       return cudaErrorInvalidValue;
   }
   const size_t smem = sizeof(Smem<NX, CH>) + 1024;
-  cudaError_t e = set_smem(gemm_mxfp4_decode_kernel<NX, CH, BF>, smem);
+  cudaError_t e = set_smem(gemm_mxfp4_decode_kernel<NX, CH, BF, Q>, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(gemm_mxfp4_decode_kernel<NX, CH, BF>, dim3(static_cast<unsigned>(p.G)),
+  // 16-byte loads of the unquantised activations where alignment allows
+  const bool vec = Q && reinterpret_cast<uintptr_t>(a.xsrc) % 16 == 0 && a.ldx % (a.xsrc_bf16 ? 8 : 4) == 0;
+  const int qflags = (a.xsrc_bf16 ? 1 : 0) | (vec ? 2 : 0);
+  return launch_pdl(gemm_mxfp4_decode_kernel<NX, CH, BF, Q>, dim3(static_cast<unsigned>(p.G)),
                     dim3(kDecThreads), smem, s, tmX, tmW, a.sfA, a.sfB, a.C, a.D, a.M, a.N, a.K, p.KS,
-                    p.U, p.smax, ws, counters);
+                    p.U, p.smax, ws, counters, a.xsrc, a.ldx, qflags);
+}
+
+template <int NX, int CH, bool Q>
+cudaError_t launch_decode_out(const Mxfp4GemmArgs& a, const decode::Plan& p, float* ws,
+                              uint32_t* counters, cudaStream_t s) {
+  return a.out_bf16 ? launch_decode_variant<NX, CH, true, Q>(a, p, ws, counters, s)
+                    : launch_decode_variant<NX, CH, false, Q>(a, p, ws, counters, s);
+}
+
+template <bool Q>
+cudaError_t launch_decode_shape(const Mxfp4GemmArgs& a, const decode::Plan& p, float* ws,
+                                uint32_t* counters, cudaStream_t s) {
+  if (p.nx == 16)
+    return p.ch == 1 ? launch_decode_out<16, 1, Q>(a, p, ws, counters, s)
+                     : launch_decode_out<16, 4, Q>(a, p, ws, counters, s);
+  return p.ch == 1 ? launch_decode_out<32, 1, Q>(a, p, ws, counters, s)
+                   : launch_decode_out<32, 2, Q>(a, p, ws, counters, s);
 }
 }  // namespace
 
@@ -826,19 +1001,8 @@ cudaError_t launch_gemm_mxfp4_decode(const Mxfp4GemmArgs& a, int num_sms, cudaSt
   float* ws = static_cast<float*>(a.workspace);
   uint32_t* counters =
       ws == nullptr ? nullptr : reinterpret_cast<uint32_t*>(ws + p.tiles * p.smax * p.nx * 128);
-  const bool bf = a.out_bf16;
-  if (p.nx == 16) {
-    if (p.ch == 1)
-      return bf ? launch_decode_variant<16, 1, true>(a, p, ws, counters, s)
-                : launch_decode_variant<16, 1, false>(a, p, ws, counters, s);
-    return bf ? launch_decode_variant<16, 4, true>(a, p, ws, counters, s)
-              : launch_decode_variant<16, 4, false>(a, p, ws, counters, s);
-  }
-  if (p.ch == 1)
-    return bf ? launch_decode_variant<32, 1, true>(a, p, ws, counters, s)
-              : launch_decode_variant<32, 1, false>(a, p, ws, counters, s);
-  return bf ? launch_decode_variant<32, 2, true>(a, p, ws, counters, s)
-            : launch_decode_variant<32, 2, false>(a, p, ws, counters, s);
+  return a.xsrc != nullptr ? launch_decode_shape<true>(a, p, ws, counters, s)
+                           : launch_decode_shape<false>(a, p, ws, counters, s);
 }
 
 }  // namespace bsg

@@ -120,11 +120,25 @@ struct Mxfp4GemmArgs {
   const void* B;
   void* workspace;           // split-K partials + tile counters (decode path)
   size_t workspace_bytes;
+  // decode path with the activations quantised in the kernel (xsrc != null):
+  // xsrc M x K, FP32 or BF16, row pitch ldx; A and sfA are not used then
+  const void* xsrc;
+  int64_t ldx;
+  bool xsrc_bf16;
 };
 cudaError_t launch_gemm_mxfp4(const Mxfp4GemmArgs& a, int num_sms, cudaStream_t s);
 // Decode-shaped (small M) MXFP4 GEMM: weights B stream once; A has M <= 32 rows.
 size_t gemm_mxfp4_decode_workspace(int M, int N, int K, int num_sms);
 cudaError_t launch_gemm_mxfp4_decode(const Mxfp4GemmArgs& a, int num_sms, cudaStream_t s);
+// MXFP4 GEMM with on-the-fly activation quantisation.  Up to kActFusedMaxM
+// activation rows the decode kernel quantises them stage by stage; above,
+// its four scale-writer warps could not keep up with the weight stream, so
+// the stand-alone quantiser runs first.  Workspace: the decode kernel's
+// split-K area (M <= 32, at off[0] = 0), then for M > kActFusedMaxM the
+// activation codes (M x K/2, at off[1]) and scale atoms (ceil(M/128) x
+// ceil(K/128) x 512 bytes, at off[2]).
+constexpr int kActFusedMaxM = 4;
+size_t gemm_mxfp4_act_workspace(int M, int N, int K, int num_sms, size_t* off);
 
 // FP4 GEMM with a BF16 or FP16 scale per 32 along K (codes [K/32][rows]),
 // promoted per K block.  A and B are packed E2M1 (rows x K/2 bytes); their

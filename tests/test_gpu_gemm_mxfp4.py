@@ -122,3 +122,72 @@ def test_mxfp4_large_kernel_ffn_up_shape_sampled():
     Dref, bnd = og.gemm_mxfp4(opa, ofa, opb, ofb)
     report("mxfp4 ffn_up sampled", *og.within_tolerance(D.float().cpu().numpy()[np.ix_(rows, cols)],
                                                         Dref, bnd, bf16=True))
+
+
+# ---- activations quantised on the fly (bsg_gemm_mxfp4_act): the result must
+# be bit for bit that of bsg_quantize_mxfp4 followed by bsg_gemm, whose
+# parity with the oracle the tests above establish; one case also goes to the
+# oracle directly.
+
+def _fused_and_separate(A, B, out, C=None, src="bf16", pad=0):
+    import torch
+    import fp4_gemm_gb300 as bsg
+    dev = device()
+    M, K = A.shape
+    xt = to_dev(A, dev)
+    if src == "bf16":
+        xt = xt.to(torch.bfloat16)
+    if pad:   # rows padded in memory: the activations are a strided view
+        buf = torch.zeros((M, K + pad), dtype=xt.dtype, device=dev)
+        buf[:, :K] = xt
+        xt = buf[:, :K]
+    pb, fb = bsg.bsg_quantize_mxfp4(to_dev(B, dev), "tcgen05")
+    Ct = None if C is None else to_dev(C, dev)
+    Df = bsg.bsg_gemm_mxfp4_act(xt, pb, fb, C=Ct, out=out)
+    assert bsg.bsg_device_error() == 0
+    pa, fa = bsg.bsg_quantize_mxfp4(xt.contiguous(), "tcgen05")
+    Ds = bsg.bsg_gemm(pa, "e2m1", fa, "mx", pb, "e2m1", fb, "mx", C=Ct, out=out)
+    assert bsg.bsg_device_error() == 0
+    return Df.float().cpu().numpy(), Ds.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("M", [1, 7, 16, 17, 32, 64])
+@pytest.mark.parametrize("N,K", [(1000, 1024), (4096, 8192), (384, 96), (2048, 2304)])
+@pytest.mark.parametrize("src", ["bf16", "f32"])
+def test_act_quantised_on_the_fly_equals_separate(M, N, K, src):
+    A, B = synth.make("decode", m=M, n=N, k=K)
+    Df, Ds = _fused_and_separate(A, B, "bf16", src=src)
+    assert np.array_equal(Df, Ds)
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_act_quantised_on_the_fly_strided_rows_addend_repeated(M):
+    # padded rows (scalar loads), an FP32 addend and FP32 output; three calls
+    # in a row reuse the workspace (its counters must come back to zero)
+    A, B = synth.make("decode", m=M, n=2048, k=4096)
+    C = synth.addend("decode", M, 2048)
+    first = None
+    for _ in range(3):
+        Df, Ds = _fused_and_separate(A, B, "f32", C=C, src="bf16", pad=8)
+        assert np.array_equal(Df, Ds)
+        if first is None:
+            first = Df
+        assert np.array_equal(Df, first)
+
+
+def test_act_quantised_on_the_fly_full_decode_shape_against_oracle():
+    # the decode benchmark shape (M=16, K=8192, N=28672), BF16 activations:
+    # all outputs equal the two-call path, sampled columns are within the
+    # oracle's tolerance
+    N, K, M = 28672, 8192, 16
+    A, B = synth.make("decode", m=M, n=N, k=K)
+    A = synth.bf16_bits_to_f32(synth.to_bf16_bits(A))
+    Df, Ds = _fused_and_separate(A, B, "bf16", src="bf16")
+    assert np.array_equal(Df, Ds)
+    rng = np.random.default_rng(11)
+    cols = np.unique(np.concatenate([np.arange(0, 4), np.arange(124, 132), np.arange(N - 4, N),
+                                     rng.integers(0, N, 128)]))
+    opa, ofa = oq.quantize_mxfp4(A)
+    opb, ofb = oq.quantize_mxfp4(B[cols])
+    Dref, bnd = og.gemm_mxfp4(opa, ofa, opb, ofb)
+    report("fused decode full size", *og.within_tolerance(Df[:, cols], Dref, bnd, bf16=True))
