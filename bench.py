@@ -74,7 +74,7 @@ L2_BYTES = 129 << 20
 
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = {"fp8": ["gemm_fp8.cu", "common.cuh", "quant_math.cuh"], "fp4": ["gemm_mxfp4.cu", "common.cuh"],
+KERNEL_SOURCES = {"fp8": ["gemm_fp8.cu", "common.cuh", "quant_math.cuh"], "fp4": ["gemm_mxfp4.cu", "common.cuh", "quant_math.cuh"],
                   "mx": ["gemm_mx.cu", "common.cuh"], "bs16": ["gemm_bs16.cu", "common.cuh"]}
 # workloads that reuse another workload's shape and seeded inputs
 SHAPE_OF = {"mxfp8_ffn_up": "ffn_up", "ffn_up_q8out": "ffn_up", "nvfp4_ffn_up": "ffn_up",
