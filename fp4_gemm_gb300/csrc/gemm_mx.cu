@@ -272,7 +272,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------------- MMA
     setmaxnreg_dec<kRegsSmall>();
     if (lane == 0 && rank == 0) {
-      uint32_t it = 0, tl = 0;
+      // The MMA queue holds little more than the running MMA, so the thread
+      // must issue a stage's first MMA while the previous stage's last two
+      // still run: everything that depends on the stage slot is a base plus
+      // the slot times a constant stride, and the slot and its phase parity
+      // advance by increments, so that little but the MMAs themselves lies
+      // between two stages.
+      const uint64_t ad0 = sdesc_kmajor_sw128(smem_u32(sm.a[0]));
+      const uint64_t bd0 = sdesc_kmajor_sw128(smem_u32(sm.b[0]));
+      constexpr uint32_t kADescStep = (BM * kRowBytes) >> 4;   // descriptor address units (16 B)
+      constexpr uint32_t kBDescStep = (KC::kBRows * kRowBytes) >> 4;
+      const uint32_t sf0 = tmem + kAccCols;
+      const int rem_last = kbytes - (KS - 1) * kRowBytes;     // 32 bytes per MMA
+      const int nk_last = rem_last >= kRowBytes ? 4 : (rem_last + 31) / 32;
+      uint32_t s = 0, ph = 0, tl = 0;    // slot and phase parity of the next stage
       bool ok = true;
       for (int t = unit; t < tiles && ok; t += units, ++tl) {
         // the epilogue has read the previous tile's accumulator
@@ -283,27 +296,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // A stage may start once its operands have landed (the scale writers
         // waited for the stage's TMA) and its scales are in tensor memory.
-        // The MMA queue holds little more than the running MMA, so work
-        // between two stages' MMAs can leave the tensor core idle: a
-        // non-blocking test of stage it+1 goes after stage it's second MMA
-        // and, if it passed, the fence after its third, where they hide under
-        // running MMAs; the commit that frees stage it follows its last MMA
-        // at once (deferring it would delay the stage's refill); a wait that
-        // may block comes only after it, when the test failed.
-        if (sm.abort_flag || !mbar_wait(smem_u32(&sm.sready[it % kStages]), (it / kStages) & 1u)) {
+        // A non-blocking test of the next stage goes after this stage's
+        // second MMA and, if it passed, the fence after its third, where they
+        // hide under running MMAs; the commit that frees this stage follows
+        // its last MMA at once (deferring it would delay the stage's refill);
+        // a wait that may block comes only after it, when the test failed.
+        if (sm.abort_flag || !mbar_wait(smem_u32(&sm.sready[s]), ph)) {
           raise_abort(&sm.abort_flag);
           break;
         }
         tc_fence_after();
-        for (int ks = 0; ks < KS && ok; ++ks, ++it) {
-          const int s = static_cast<int>(it % kStages);
-          const uint32_t sfa_t = tmem + kAccCols + s * kSfColsPerStage;
+        for (int ks = 0; ks < KS && ok; ++ks) {
+          const uint32_t sfa_t = sf0 + s * kSfColsPerStage;
           const uint32_t sfb_t = sfa_t + KC::kSfbOff;
-          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sm.a[s]));
-          const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sm.b[s]));
-          const int rem = kbytes - ks * kRowBytes;           // 32 bytes per MMA
-          const int nk = rem >= kRowBytes ? 4 : (rem + 31) / 32;
+          const uint64_t ad = ad0 + s * kADescStep;
+          const uint64_t bd = bd0 + s * kBDescStep;
           const bool more = ks + 1 < KS;
+          const int nk = more ? 4 : nk_last;
+          const uint32_t s1 = s + 1 == static_cast<uint32_t>(kStages) ? 0u : s + 1;
+          const uint32_t ph1 = s1 == 0 ? ph ^ 1u : ph;
           bool next_ready = false;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
@@ -337,8 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            acc);
               }
             }
-            if (kk == 1 && more)
-              next_ready = mbar_test(smem_u32(&sm.sready[(it + 1) % kStages]), ((it + 1) / kStages) & 1u);
+            if (kk == 1 && more) next_ready = mbar_test(smem_u32(&sm.sready[s1]), ph1);
             if (kk == 2 && next_ready) tc_fence_after();
           }
           if (kPair)
@@ -346,12 +356,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             tc_commit(smem_u32(&sm.done[s]));
           if (more && !next_ready) {
-            if (!mbar_wait(smem_u32(&sm.sready[(it + 1) % kStages]), ((it + 1) / kStages) & 1u)) {
+            if (!mbar_wait(smem_u32(&sm.sready[s1]), ph1)) {
               raise_abort(&sm.abort_flag);
               ok = false;
             }
             tc_fence_after();
           }
+          s = s1;
+          ph = ph1;
         }
         if (!ok) break;
         if (kPair)
