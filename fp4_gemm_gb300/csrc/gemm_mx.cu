@@ -287,13 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nk_last = rem_last >= kRowBytes ? 4 : (rem_last + 31) / 32;
       uint32_t s = 0, ph = 0, tl = 0;    // slot and phase parity of the next stage
       bool ok = true;
+      bool next_ready = false;           // the next stage's scales are known to be in place
       for (int t = unit; t < tiles && ok; t += units, ++tl) {
-        // the epilogue has read the previous tile's accumulator
-        if (!mbar_wait(smem_u32(&sm.tempty), (tl & 1u) ^ 1u)) {
-          raise_abort(&sm.abort_flag);
-          break;
-        }
-        tc_fence_after();
         // A stage may start once its operands have landed (the scale writers
         // waited for the stage's TMA) and its scales are in tensor memory.
         // A non-blocking test of the next stage goes after this stage's
@@ -301,7 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // hide under running MMAs; the commit that frees this stage follows
         // its last MMA at once (deferring it would delay the stage's refill);
         // a wait that may block comes only after it, when the test failed.
-        if (sm.abort_flag || !mbar_wait(smem_u32(&sm.sready[s]), ph)) {
+        // A tile's last stage tests the next tile's first, so that a new tile
+        // waits only for the epilogue to have read the accumulator.
+        if (!mbar_wait(smem_u32(&sm.tempty), (tl & 1u) ^ 1u) ||
+            (!next_ready && (sm.abort_flag || !mbar_wait(smem_u32(&sm.sready[s]), ph)))) {
           raise_abort(&sm.abort_flag);
           break;
         }
@@ -315,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nk = more ? 4 : nk_last;
           const uint32_t s1 = s + 1 == static_cast<uint32_t>(kStages) ? 0u : s + 1;
           const uint32_t ph1 = s1 == 0 ? ph ^ 1u : ph;
-          bool next_ready = false;
+          next_ready = false;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             if (kk < nk) {
@@ -348,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            acc);
               }
             }
-            if (kk == 1 && more) next_ready = mbar_test(smem_u32(&sm.sready[s1]), ph1);
+            if (kk == 1) next_ready = mbar_test(smem_u32(&sm.sready[s1]), ph1);
             if (kk == 2 && next_ready) tc_fence_after();
           }
           if (kPair)
