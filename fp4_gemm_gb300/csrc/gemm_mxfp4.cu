@@ -511,6 +511,42 @@ __device__ __forceinline__ void store_row(const float (&v)[NX], const float* __r
   }
 }
 
+// Prefetch of a tensor-map box (same coordinates as the load it stands in
+// front of) or of `bytes` of global memory (multiple of 16, 16-byte aligned)
+// into L2.  A hint only: nothing completes and no data reaches the CTA.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x),
+               "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// L2 prefetch of the weight boxes and weight-scale atoms of a decode CTA's
+// first `stages` units (the coordinates its producer and scale writers load
+// them with).  Not inlined: its registers stay out of the kernel's roles.
+__device__ __noinline__ void prefetch_first_stages(const CUtensorMap* tmW, const uint8_t* sfW, int64_t u0,
+                                                   int64_t u1, int64_t KS, int KA, int stages, int CH) {
+  const int64_t npf = u1 - u0 < stages ? u1 - u0 : stages;
+  for (int64_t i = 0; i < npf; ++i) {
+    const int64_t u = u0 + i;
+    const int64_t tile = u / KS;
+    const int c0 = static_cast<int>(u % KS) * CH;
+    if (CH == 1)
+      tma_prefetch_l2_2d(tmW, c0 * kRowBytes, static_cast<int32_t>(tile * 128));
+    else
+      tma_prefetch_l2_3d(tmW, 0, static_cast<int32_t>(tile * 128), c0);
+    const int ka0 = 2 * c0;
+    const int na = min(2 * CH, KA - ka0);
+    if (na > 0) bulk_prefetch_l2(sfW + (tile * KA + ka0) * kSfAtom, static_cast<uint32_t>(na * kSfAtom));
+  }
+}
+
 // kQ: the activations arrive unquantised (FP32 or BF16, xsrc with row pitch
 // ldx; qflags bit 0: BF16, bit 1: 16-byte loads allowed) and are quantised
 // stage by stage by the scale-writer warps: each stage's K slice of all
@@ -571,6 +607,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   grid_dep_launch();
+  // The weights and weight scales of the first stages go into L2 before the
+  // wait for the previous kernel, so that under programmatic dependent
+  // launch their DRAM latency overlaps that kernel's tail.  A prefetch only
+  // moves lines into L2, where every SM's writes land: the loads after the
+  // wait see whatever the previous kernel wrote, prefetched or not.
+  if (warp == kProducerWarp && lane == 0) prefetch_first_stages(&tmW, sfW, u0, u1, KS, KA, kStages, CH);
   grid_dep_wait();
 
   if (warp == kProducerWarp) {
