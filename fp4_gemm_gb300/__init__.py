@@ -35,7 +35,7 @@ EXPORTS = ("bsg_quantize_fp8", "bsg_quantize_mxfp4", "bsg_gemm", "bsg_gemm_works
            "bsg_num_sms", "bsg_gemm_decode_noalloc", "bsg_mma_peak", "bsg_quantize_mx",
            "bsg_mma_probe", "bsg_gemm_quantized", "bsg_quantize_nvfp4", "bsg_gemm_nvfp4",
            "bsg_check_wait_timeout", "bsg_quantize_fp4_bs16", "bsg_mma_probe_mx",
-           "bsg_gemm_mxfp4_act", "bsg_gemm_mxfp4_act_workspace_size")
+           "bsg_gemm_mxfp4_act", "bsg_gemm_mxfp4_act_workspace_size", "bsg_gemm_nvfp4_ws")
 
 
 class BsgError(RuntimeError):
@@ -93,6 +93,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bsg_quantize_fp4_bs16.restype = i32
     lib.bsg_gemm_nvfp4.argtypes = [i64, i64, i64, vp, vp, vp, vp, f32, vp, vp, i32, vp]
     lib.bsg_gemm_nvfp4.restype = i32
+    lib.bsg_gemm_nvfp4_ws.argtypes = [i64, i64, i64, vp, vp, vp, vp, f32, vp, vp, i32, vp, sz, vp]
+    lib.bsg_gemm_nvfp4_ws.restype = i32
     lib.bsg_check_wait_timeout.argtypes = [vp]
     lib.bsg_check_wait_timeout.restype = i32
     lib.bsg_mma_peak.argtypes = [i32, i32, i32, i64, c.POINTER(i64), vp]
@@ -326,9 +328,12 @@ def bsg_quantize_fp4_bs16(x: torch.Tensor, scale: str = "bf16", q: torch.Tensor 
 
 def bsg_gemm_nvfp4(A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor, sB: torch.Tensor,
                    alpha: float = 1.0, C: torch.Tensor | None = None, out: str = "f32",
-                   D: torch.Tensor | None = None, K: int | None = None, stream=None):
+                   D: torch.Tensor | None = None, K: int | None = None,
+                   workspace: torch.Tensor | None = None, stream=None):
     """D = alpha * sum_k (s_A a_k)(s_B b_k) + C for NVFP4 operands: A (M, K/2)
-    and B (N, K/2) packed, sA / sB E4M3 scales in the tcgen05 layout."""
+    and B (N, K/2) packed, sA / sB E4M3 scales in the tcgen05 layout.  Calls
+    bsg_gemm_nvfp4_ws with the workspace bsg_gemm would use (cached per
+    device), so that up to 32 rows take the decode-shaped kernel."""
     lib = load_library()
     M, N = A.shape[0], B.shape[0]
     if K is None:
@@ -336,10 +341,13 @@ def bsg_gemm_nvfp4(A: torch.Tensor, sA: torch.Tensor, B: torch.Tensor, sB: torch
     if D is None:
         D = torch.empty((M, N), dtype=torch.float32 if out == "f32" else torch.bfloat16,
                         device=A.device)
-    _need_cuda(A, sA, B, sB, C, D)
-    _check(lib.bsg_gemm_nvfp4(M, N, K, _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), float(alpha), _ptr(C),
-                              _ptr(D), DTYPE[out], _stream(stream)),
-           "bsg_gemm_nvfp4")
+    if workspace is None:
+        workspace = workspace_for(M, N, K, "e2m1", "e2m1", A.device)
+    _need_cuda(A, sA, B, sB, C, D, workspace)
+    _check(lib.bsg_gemm_nvfp4_ws(M, N, K, _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), float(alpha), _ptr(C),
+                                 _ptr(D), DTYPE[out], _ptr(workspace),
+                                 0 if workspace is None else workspace.numel(), _stream(stream)),
+           "bsg_gemm_nvfp4_ws")
     return D
 
 

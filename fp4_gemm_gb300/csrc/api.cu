@@ -494,15 +494,12 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
     a.workspace_bytes = workspace_bytes;
     a.A = A;
     a.B = B;
+    // NVFP4 through this entry point: tensor scales are folded into alpha by
+    // bsg_gemm_nvfp4, so alpha is 1 here
     const bool nv = ga == BSG_SCALE_BLOCK1x16_E4M3;
-    if ((nv || M > kDecodeMaxM) && bsg::gemm_mx_fp4_large(a.M, a.N, sms))
-      return run_fp4_large(nv ? 2 : 1, 1.0f, M, N, K, A, sA, B, sB, C, D, out == BSG_BF16, sms, s);
-    if (nv) {
-      // NVFP4 below the large-kernel size: the general kernel (no decode
-      // path); tensor scales are folded into alpha by bsg_gemm_nvfp4 (1 here)
-      a.nvfp4 = true;
-      a.alpha = 1.0f;
-    } else if (M <= kDecodeMaxM) {
+    a.nvfp4 = nv;
+    a.alpha = 1.0f;
+    if (M <= kDecodeMaxM) {
       const size_t need = bsg::gemm_mxfp4_decode_workspace(a.M, a.N, a.K, sms);
       if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)))
         return BSG_ERR_WORKSPACE;
@@ -510,6 +507,8 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
       // launcher encodes its own tensor maps
       return from_cuda(bsg::launch_gemm_mxfp4_decode(a, sms, s));
     }
+    if (bsg::gemm_mx_fp4_large(a.M, a.N, sms))
+      return run_fp4_large(nv ? 2 : 1, 1.0f, M, N, K, A, sA, B, sB, C, D, out == BSG_BF16, sms, s);
     if (!make_kmajor_map(&a.tmA, A, K / 2, M, K / 2, 128) ||
         !make_kmajor_map(&a.tmB, B, K / 2, N, K / 2, 128))
       return BSG_ERR_CUDA;
@@ -520,6 +519,12 @@ bsg_status bsg_gemm(int64_t M, int64_t N, int64_t K, const void* A, bsg_format f
 bsg_status bsg_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const void* A, const void* sA,
                           const void* B, const void* sB, float alpha, const float* C, void* D,
                           bsg_dtype out, void* stream) {
+  return bsg_gemm_nvfp4_ws(M, N, K, A, sA, B, sB, alpha, C, D, out, nullptr, 0, stream);
+}
+
+bsg_status bsg_gemm_nvfp4_ws(int64_t M, int64_t N, int64_t K, const void* A, const void* sA,
+                             const void* B, const void* sB, float alpha, const float* C, void* D,
+                             bsg_dtype out, void* workspace, size_t workspace_bytes, void* stream) {
   if (A == nullptr || B == nullptr || sA == nullptr || sB == nullptr || D == nullptr)
     return BSG_ERR_INVALID_ARG;
   if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || K % 32)
@@ -533,8 +538,6 @@ bsg_status bsg_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const void* A, const 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int sms = num_sms_current();
   if (sms <= 0) return BSG_ERR_CUDA;
-  if (bsg::gemm_mx_fp4_large(static_cast<int>(M), static_cast<int>(N), sms))
-    return run_fp4_large(2, alpha, M, N, K, A, sA, B, sB, C, D, out == BSG_BF16, sms, s);
   Mxfp4GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.M = static_cast<int>(M);
@@ -549,6 +552,19 @@ bsg_status bsg_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const void* A, const 
   a.out_bf16 = out == BSG_BF16;
   a.A = A;
   a.B = B;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  if (M <= kDecodeMaxM) {
+    // the decode-shaped kernel (weights streamed once, split over all SMs)
+    // when its split-K workspace is given or not needed; without a
+    // workspace the general kernel below serves the call
+    const size_t need = bsg::gemm_mxfp4_decode_workspace(a.M, a.N, a.K, sms);
+    const bool have = workspace != nullptr && workspace_bytes >= need && aligned(workspace, 16);
+    if (need == 0 || have) return from_cuda(bsg::launch_gemm_mxfp4_decode(a, sms, s));
+    if (workspace != nullptr) return BSG_ERR_WORKSPACE;
+  }
+  if (bsg::gemm_mx_fp4_large(static_cast<int>(M), static_cast<int>(N), sms))
+    return run_fp4_large(2, alpha, M, N, K, A, sA, B, sB, C, D, out == BSG_BF16, sms, s);
   if (!make_kmajor_map(&a.tmA, A, K / 2, M, K / 2, 128) ||
       !make_kmajor_map(&a.tmB, B, K / 2, N, K / 2, 128))
     return BSG_ERR_CUDA;

@@ -345,12 +345,16 @@ constexpr int kSlab = 128 * kRowBytes;   // one 128-row x 128-byte weight slab
 // hundred ns), while each of its M128 x N16 x K64 MMAs takes ~30 ns.
 __host__ __device__ constexpr int pow2_at_least(int v, int p) { return p >= v ? p : pow2_at_least(v, 2 * p); }
 
-template <int NX, int CH>
+template <int NX, int CH, bool kNv = false>
 struct Cfg {
   static constexpr int kStageBytes = CH * (kSlab + NX * kRowBytes);
   static constexpr int kStages0 = (216 * 1024) / kStageBytes;
   static constexpr int kStages = kStages0 > 12 ? 12 : kStages0;
-  static constexpr int kSfColsPerStage = CH * 16;   // per chunk: SFW 2 atoms + SFX 2 atoms
+  // scale atoms per 128-byte chunk and operand: MXFP4 two (E8M0 per 32),
+  // NVFP4 four (UE4M3 per 16); per chunk the weights' atoms, then the
+  // activations', four columns each
+  static constexpr int kAtomsPerChunk = kNv ? 4 : 2;
+  static constexpr int kSfColsPerStage = CH * 8 * kAtomsPerChunk;
   static constexpr int kSfBase = 2 * NX;            // after the two accumulator buffers
   static constexpr int kTmemCols = pow2_at_least(kSfBase + kStages * kSfColsPerStage, 32);
   static_assert(kStages >= 2, "at least two stages");
@@ -494,15 +498,21 @@ __device__ __forceinline__ uint32_t swz128_piece(int r, int p) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + (((p ^ r) & 7) << 4));
 }
 
-template <int NX, bool kBF16Out>
+// NVFP4: alpha * acc + C with one rounding (alpha * acc without C), as the
+// other NVFP4 kernels do; MXFP4: acc + C
+template <int NX, bool kBF16Out, bool kNv>
 __device__ __forceinline__ void store_row(const float (&v)[NX], const float* __restrict__ Cin,
-                                          void* __restrict__ Dout, int M, int N, int64_t n) {
+                                          void* __restrict__ Dout, int M, int N, int64_t n, float alpha) {
   if (n >= N) return;
 #pragma unroll
   for (int mm = 0; mm < NX; ++mm) {
     if (mm < M) {
       float o = v[mm];
-      if (Cin != nullptr) o += __ldg(Cin + static_cast<int64_t>(mm) * N + n);
+      if (kNv)
+        o = Cin != nullptr ? __fmaf_rn(o, alpha, __ldg(Cin + static_cast<int64_t>(mm) * N + n))
+                           : __fmul_rn(o, alpha);
+      else if (Cin != nullptr)
+        o = __fadd_rn(o, __ldg(Cin + static_cast<int64_t>(mm) * N + n));
       if (kBF16Out)
         static_cast<__nv_bfloat16*>(Dout)[static_cast<int64_t>(mm) * N + n] = __float2bfloat16_rn(o);
       else
@@ -531,7 +541,8 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
 // first `stages` units (the coordinates its producer and scale writers load
 // them with).  Not inlined: its registers stay out of the kernel's roles.
 __device__ __noinline__ void prefetch_first_stages(const CUtensorMap* tmW, const uint8_t* sfW, int64_t u0,
-                                                   int64_t u1, int64_t KS, int KA, int stages, int CH) {
+                                                   int64_t u1, int64_t KS, int KA, int stages, int CH,
+                                                   int apc) {
   const int64_t npf = u1 - u0 < stages ? u1 - u0 : stages;
   for (int64_t i = 0; i < npf; ++i) {
     const int64_t u = u0 + i;
@@ -541,8 +552,8 @@ __device__ __noinline__ void prefetch_first_stages(const CUtensorMap* tmW, const
       tma_prefetch_l2_2d(tmW, c0 * kRowBytes, static_cast<int32_t>(tile * 128));
     else
       tma_prefetch_l2_3d(tmW, 0, static_cast<int32_t>(tile * 128), c0);
-    const int ka0 = 2 * c0;
-    const int na = min(2 * CH, KA - ka0);
+    const int ka0 = apc * c0;
+    const int na = min(apc * CH, KA - ka0);
     if (na > 0) bulk_prefetch_l2(sfW + (tile * KA + ka0) * kSfAtom, static_cast<uint32_t>(na * kSfAtom));
   }
 }
@@ -555,7 +566,7 @@ __device__ __noinline__ void prefetch_first_stages(const CUtensorMap* tmW, const
 // and E8M0 codes stored into the tensor-memory scale cells - so the TMA
 // moves weights only, and no other kernel or CTA is waited for.  tmX and sfX
 // are not used then.
-template <int NX, int CH, bool kBF16Out, bool kQ>
+template <int NX, int CH, bool kBF16Out, bool kQ, bool kNv>
 __global__ void __launch_bounds__(kDecThreads, 1)
     gemm_mxfp4_decode_kernel(const __grid_constant__ CUtensorMap tmX,
                              const __grid_constant__ CUtensorMap tmW,
@@ -563,11 +574,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                              const float* __restrict__ Cin, void* __restrict__ Dout, int M, int N,
                              int K, int64_t KS, int64_t U, int64_t smax,
                              float* __restrict__ ws, uint32_t* __restrict__ counters,
-                             const void* __restrict__ xsrc, int64_t ldx, int qflags) {
-  constexpr int kStages = Cfg<NX, CH>::kStages;
-  constexpr int kSfCols = Cfg<NX, CH>::kSfColsPerStage;
-  constexpr int kSfBase = Cfg<NX, CH>::kSfBase;
-  constexpr int kTmemCols = Cfg<NX, CH>::kTmemCols;
+                             const void* __restrict__ xsrc, int64_t ldx, int qflags, float alpha) {
+  static_assert(!(kQ && kNv), "activations are quantised in the kernel for MXFP4 only");
+  constexpr int kStages = Cfg<NX, CH, kNv>::kStages;
+  constexpr int kSfCols = Cfg<NX, CH, kNv>::kSfColsPerStage;
+  constexpr int kSfBase = Cfg<NX, CH, kNv>::kSfBase;
+  constexpr int kTmemCols = Cfg<NX, CH, kNv>::kTmemCols;
+  constexpr int kApc = Cfg<NX, CH, kNv>::kAtomsPerChunk;
   extern __shared__ uint8_t smem_raw[];
   Smem<NX, CH>& sm = *reinterpret_cast<Smem<NX, CH>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -578,7 +591,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const int64_t u1 = (static_cast<int64_t>(blockIdx.x) + 1) * U / G;
   const int kbytes = K / 2;
   const int KC = (kbytes + kRowBytes - 1) / kRowBytes;   // 128-byte chunks along K
-  const int KA = (K / 32 + 3) / 4;                       // scale atoms along K
+  const int KA = (K / (kNv ? 16 : 32) + 3) / 4;          // scale atoms along K
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -612,7 +625,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   // launch their DRAM latency overlaps that kernel's tail.  A prefetch only
   // moves lines into L2, where every SM's writes land: the loads after the
   // wait see whatever the previous kernel wrote, prefetched or not.
-  if (warp == kProducerWarp && lane == 0) prefetch_first_stages(&tmW, sfW, u0, u1, KS, KA, kStages, CH);
+  if (warp == kProducerWarp && lane == 0) prefetch_first_stages(&tmW, sfW, u0, u1, KS, KA, kStages, CH, kApc);
   grid_dep_wait();
 
   if (warp == kProducerWarp) {
@@ -681,12 +694,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           const uint64_t x0 = sdesc_kmajor_sw128(smem_u32(sm.x[s]));
 #pragma unroll
           for (int j = 0; j < CH; ++j) {
+            const uint32_t sfj = sfc + 8 * kApc * j;   // chunk j: weight atoms, then activation atoms
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              mma_mxf4(d, w0 + (j * kSlab) / 16 + 2 * kk, x0 + (j * NX * kRowBytes) / 16 + 2 * kk,
-                       idesc_mxf4(128, NX, (kk & 1) * 2, (kk & 1) * 2),
-                       sfc + 16 * j + 4 * (kk >> 1), sfc + 16 * j + 8 + 4 * (kk >> 1),
-                       (j == 0 && kk == 0) ? acc0 : 1u);
+              const uint64_t wd = w0 + (j * kSlab) / 16 + 2 * kk;
+              const uint64_t xd = x0 + (j * NX * kRowBytes) / 16 + 2 * kk;
+              const uint32_t acc = (j == 0 && kk == 0) ? acc0 : 1u;
+              if (kNv)   // K = 64 = one atom (four UE4M3 bytes per row) per MMA
+                mma_nvf4(d, wd, xd, idesc_nvf4(128, NX), sfj + 4 * kk, sfj + 4 * kApc + 4 * kk, acc);
+              else       // K = 64 = half an E8M0 atom: the scale id picks bytes 0-1 or 2-3
+                mma_mxf4(d, wd, xd, idesc_mxf4(128, NX, (kk & 1) * 2, (kk & 1) * 2), sfj + 4 * (kk >> 1),
+                         sfj + 4 * kApc + 4 * (kk >> 1), acc);
             }
           }
         } else {
@@ -696,11 +714,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             const uint64_t xd = sdesc_kmajor_sw128(smem_u32(sm.x[s] + j * NX * kRowBytes));
             const int rem = kbytes - (c0 + j) * kRowBytes;
             const int nk = min(4, (rem + 31) / 32);
-            const uint32_t sfj = sfc + 16 * j;
+            const uint32_t sfj = sfc + 8 * kApc * j;
             for (int kk = 0; kk < nk; ++kk) {
-              const uint32_t id = idesc_mxf4(128, NX, (kk & 1) * 2, (kk & 1) * 2);
-              mma_mxf4(d, wd + 2 * kk, xd + 2 * kk, id, sfj + 4 * (kk >> 1), sfj + 8 + 4 * (kk >> 1),
-                       (j == 0 && kk == 0) ? acc0 : 1u);
+              const uint32_t acc = (j == 0 && kk == 0) ? acc0 : 1u;
+              if (kNv) {
+                mma_nvf4(d, wd + 2 * kk, xd + 2 * kk, idesc_nvf4(128, NX), sfj + 4 * kk, sfj + 4 * kApc + 4 * kk,
+                         acc);
+              } else {
+                const uint32_t id = idesc_mxf4(128, NX, (kk & 1) * 2, (kk & 1) * 2);
+                mma_mxf4(d, wd + 2 * kk, xd + 2 * kk, id, sfj + 4 * (kk >> 1), sfj + 4 * kApc + 4 * (kk >> 1),
+                         acc);
+              }
             }
           }
         }
@@ -734,65 +758,87 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
       tc_fence_after();
       const int64_t tile = u / KS;
-      const int ka0 = 2 * static_cast<int>(u % KS) * CH;
-      const int na = min(2 * CH, KA - ka0);
+      const int ka0 = kApc * static_cast<int>(u % KS) * CH;
+      const int na = min(kApc * CH, KA - ka0);
       const uint4* gw = reinterpret_cast<const uint4*>(sfW + (tile * KA + ka0) * kSfAtom) + lane;
       const uint4* gx = reinterpret_cast<const uint4*>(sfX + static_cast<int64_t>(ka0) * kSfAtom) + lane;
-      uint4 vw[2 * CH], vx[2 * CH];
-#pragma unroll
-      for (int a = 0; a < 2 * CH; ++a)
-        if (a < na) vw[a] = __ldg(gw + a * (kSfAtom / 16));
-      if constexpr (kQ) {
-        // This stage's K slice (CH x 256 values) of every activation row,
-        // one 32-value block per item, items row-major so that neighbouring
-        // threads read neighbouring bytes.  Rows past M and blocks past K/32
-        // get zero codes and scale code 127, as a TMA load past the edge
-        // and the stand-alone quantiser's padding give.
-        constexpr int kBlocks = 8 * CH;                 // 32-value blocks in the slice
-        constexpr int kItems = NX * kBlocks / 128;      // per thread
-        static_assert(NX * kBlocks % 128 == 0, "whole items per thread");
-        const int t = static_cast<int>(threadIdx.x) - kSfWarp0 * 32;
-        const int64_t gb0 = static_cast<int64_t>(u % KS) * CH * 8;   // first block of the slice
-        const int buf = static_cast<int>(it & 1u);
-        uint8_t* xs = sm.x[s];
-#pragma unroll
-        for (int j = 0; j < kItems; ++j) {
-          const int i = t + 128 * j;
-          const int r = i / kBlocks, bb = i % kBlocks;
-          const int64_t gb = gb0 + bb;
-          uint4 codes = make_uint4(0u, 0u, 0u, 0u);
-          uint32_t code = 127u;
-          if (r < M && gb < K / 32)
-            code = quantize_block_mxfp4(xsrc, (qflags & 1) != 0, (qflags & 2) != 0, ldx, r, gb, codes);
-          st_shared_v4(smem_u32(xs + (bb >> 3) * NX * kRowBytes) + swz128_piece(r, bb & 7), codes);
-          reinterpret_cast<uint8_t*>(&sm.xsc[buf][bb >> 2][r])[bb & 3] = static_cast<uint8_t>(code);
-        }
-        fence_proxy_async_smem();   // the codes are read by the tensor core (async proxy)
-        // all four scale-writer warps have written this stage's codes (a
-        // bounded wait: a warp that stopped on an abort cannot hang the rest);
-        // buffer it & 1 comes round again two stages later, after every
-        // thread has arrived on the stage in between, i.e. read this one
-        mbar_arrive(smem_u32(&sm.xbar[buf]));
-        if (!mbar_wait(smem_u32(&sm.xbar[buf]), (it >> 1) & 1u)) {
-          raise_abort(&sm.abort_flag);
-          break;
-        }
-#pragma unroll
-        for (int a = 0; a < 2 * CH; ++a)
-          if (a < na)
-            vx[a] = make_uint4(lane < NX ? sm.xsc[buf][a][lane] : 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu,
-                               0x7F7F7F7Fu);
-      } else {
-#pragma unroll
-        for (int a = 0; a < 2 * CH; ++a)
-          if (a < na) vx[a] = __ldg(gx + a * (kSfAtom / 16));
-      }
       const uint32_t sfc = lane_base + kSfBase + s * kSfCols;
+      if constexpr (kNv) {
+        // NVFP4: every load of the stage's atoms is issued before the first
+        // store, so the stage waits for one memory latency, not one per
+        // chunk (chunk j: weight atoms at columns 32 j + 4 q, activation
+        // atoms 16 columns later)
+        uint4 vw[4 * CH], vx[4 * CH];
 #pragma unroll
-      for (int a = 0; a < 2 * CH; ++a) {
-        if (a < na) {
-          tmem_st_4(sfc + 16 * (a >> 1) + 4 * (a & 1), vw[a]);
-          tmem_st_4(sfc + 16 * (a >> 1) + 8 + 4 * (a & 1), vx[a]);
+        for (int a = 0; a < 4 * CH; ++a) {
+          if (a < na) {
+            vw[a] = __ldg(gw + a * (kSfAtom / 16));
+            vx[a] = __ldg(gx + a * (kSfAtom / 16));
+          }
+        }
+#pragma unroll
+        for (int a = 0; a < 4 * CH; ++a) {
+          if (a < na) {
+            tmem_st_4(sfc + 32 * (a >> 2) + 4 * (a & 3), vw[a]);
+            tmem_st_4(sfc + 32 * (a >> 2) + 16 + 4 * (a & 3), vx[a]);
+          }
+        }
+      } else {
+        uint4 vw[2 * CH], vx[2 * CH];
+#pragma unroll
+        for (int a = 0; a < 2 * CH; ++a)
+          if (a < na) vw[a] = __ldg(gw + a * (kSfAtom / 16));
+        if constexpr (kQ) {
+          // This stage's K slice (CH x 256 values) of every activation row,
+          // one 32-value block per item, items row-major so that neighbouring
+          // threads read neighbouring bytes.  Rows past M and blocks past K/32
+          // get zero codes and scale code 127, as a TMA load past the edge
+          // and the stand-alone quantiser's padding give.
+          constexpr int kBlocks = 8 * CH;                 // 32-value blocks in the slice
+          constexpr int kItems = NX * kBlocks / 128;      // per thread
+          static_assert(NX * kBlocks % 128 == 0, "whole items per thread");
+          const int t = static_cast<int>(threadIdx.x) - kSfWarp0 * 32;
+          const int64_t gb0 = static_cast<int64_t>(u % KS) * CH * 8;   // first block of the slice
+          const int buf = static_cast<int>(it & 1u);
+          uint8_t* xs = sm.x[s];
+#pragma unroll
+          for (int j = 0; j < kItems; ++j) {
+            const int i = t + 128 * j;
+            const int r = i / kBlocks, bb = i % kBlocks;
+            const int64_t gb = gb0 + bb;
+            uint4 codes = make_uint4(0u, 0u, 0u, 0u);
+            uint32_t code = 127u;
+            if (r < M && gb < K / 32)
+              code = quantize_block_mxfp4(xsrc, (qflags & 1) != 0, (qflags & 2) != 0, ldx, r, gb, codes);
+            st_shared_v4(smem_u32(xs + (bb >> 3) * NX * kRowBytes) + swz128_piece(r, bb & 7), codes);
+            reinterpret_cast<uint8_t*>(&sm.xsc[buf][bb >> 2][r])[bb & 3] = static_cast<uint8_t>(code);
+          }
+          fence_proxy_async_smem();   // the codes are read by the tensor core (async proxy)
+          // all four scale-writer warps have written this stage's codes (a
+          // bounded wait: a warp that stopped on an abort cannot hang the rest);
+          // buffer it & 1 comes round again two stages later, after every
+          // thread has arrived on the stage in between, i.e. read this one
+          mbar_arrive(smem_u32(&sm.xbar[buf]));
+          if (!mbar_wait(smem_u32(&sm.xbar[buf]), (it >> 1) & 1u)) {
+            raise_abort(&sm.abort_flag);
+            break;
+          }
+#pragma unroll
+          for (int a = 0; a < 2 * CH; ++a)
+            if (a < na)
+              vx[a] = make_uint4(lane < NX ? sm.xsc[buf][a][lane] : 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu,
+                                 0x7F7F7F7Fu);
+        } else {
+#pragma unroll
+          for (int a = 0; a < 2 * CH; ++a)
+            if (a < na) vx[a] = __ldg(gx + a * (kSfAtom / 16));
+        }
+#pragma unroll
+        for (int a = 0; a < 2 * CH; ++a) {
+          if (a < na) {
+            tmem_st_4(sfc + 16 * (a >> 1) + 4 * (a & 1), vw[a]);
+            tmem_st_4(sfc + 16 * (a >> 1) + 8 + 4 * (a & 1), vx[a]);
+          }
         }
       }
       tc_wait_st();
@@ -869,7 +915,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.tempty[buf]));
       if (whole) {
-        store_row<NX, kBF16Out>(acc, Cin, Dout, M, N, n);
+        store_row<NX, kBF16Out, kNv>(acc, Cin, Dout, M, N, n, alpha);
       } else if (fast) {
         float tot[NX];
 #pragma unroll
@@ -879,7 +925,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           for (int i = 0; i < 2; ++i)
             if (i < nsuf) tot[mm] += suf[i][mm];
         }
-        store_row<NX, kBF16Out>(tot, Cin, Dout, M, N, n);
+        store_row<NX, kBF16Out, kNv>(tot, Cin, Dout, M, N, n, alpha);
         // leave the workspace zero-filled for the next call
         float* base = ws + tile * smax * NX * 128 + row;
         for (int64_t sg = 0; sg < nseg; ++sg) {
@@ -917,7 +963,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
               *slot = 0.0f;
             }
           }
-          store_row<NX, kBF16Out>(tot, Cin, Dout, M, N, n);
+          store_row<NX, kBF16Out, kNv>(tot, Cin, Dout, M, N, n, alpha);
           if (threadIdx.x == 0) atomicExch(counters + tile, 0u);
         }
       }
@@ -993,7 +1039,7 @@ size_t gemm_mxfp4_act_workspace(int M, int N, int K, int num_sms, size_t* off) {
 }
 
 namespace {
-template <int NX, int CH, bool BF, bool Q>
+template <int NX, int CH, bool BF, bool Q, bool NV>
 cudaError_t launch_decode_variant(const Mxfp4GemmArgs& a, const decode::Plan& p, float* ws,
                                   uint32_t* counters, cudaStream_t s) {
   using namespace decode;
@@ -1009,31 +1055,31 @@ cudaError_t launch_decode_variant(const Mxfp4GemmArgs& a, const decode::Plan& p,
       return cudaErrorInvalidValue;
   }
   const size_t smem = sizeof(Smem<NX, CH>) + 1024;
-  cudaError_t e = set_smem(gemm_mxfp4_decode_kernel<NX, CH, BF, Q>, smem);
+  cudaError_t e = set_smem(gemm_mxfp4_decode_kernel<NX, CH, BF, Q, NV>, smem);
   if (e != cudaSuccess) return e;
   // 16-byte loads of the unquantised activations where alignment allows
   const bool vec = Q && reinterpret_cast<uintptr_t>(a.xsrc) % 16 == 0 && a.ldx % (a.xsrc_bf16 ? 8 : 4) == 0;
   const int qflags = (a.xsrc_bf16 ? 1 : 0) | (vec ? 2 : 0);
-  return launch_pdl(gemm_mxfp4_decode_kernel<NX, CH, BF, Q>, dim3(static_cast<unsigned>(p.G)),
+  return launch_pdl(gemm_mxfp4_decode_kernel<NX, CH, BF, Q, NV>, dim3(static_cast<unsigned>(p.G)),
                     dim3(kDecThreads), smem, s, tmX, tmW, a.sfA, a.sfB, a.C, a.D, a.M, a.N, a.K, p.KS,
-                    p.U, p.smax, ws, counters, a.xsrc, a.ldx, qflags);
+                    p.U, p.smax, ws, counters, a.xsrc, a.ldx, qflags, NV ? a.alpha : 1.0f);
 }
 
-template <int NX, int CH, bool Q>
+template <int NX, int CH, bool Q, bool NV>
 cudaError_t launch_decode_out(const Mxfp4GemmArgs& a, const decode::Plan& p, float* ws,
                               uint32_t* counters, cudaStream_t s) {
-  return a.out_bf16 ? launch_decode_variant<NX, CH, true, Q>(a, p, ws, counters, s)
-                    : launch_decode_variant<NX, CH, false, Q>(a, p, ws, counters, s);
+  return a.out_bf16 ? launch_decode_variant<NX, CH, true, Q, NV>(a, p, ws, counters, s)
+                    : launch_decode_variant<NX, CH, false, Q, NV>(a, p, ws, counters, s);
 }
 
-template <bool Q>
+template <bool Q, bool NV>
 cudaError_t launch_decode_shape(const Mxfp4GemmArgs& a, const decode::Plan& p, float* ws,
                                 uint32_t* counters, cudaStream_t s) {
   if (p.nx == 16)
-    return p.ch == 1 ? launch_decode_out<16, 1, Q>(a, p, ws, counters, s)
-                     : launch_decode_out<16, 4, Q>(a, p, ws, counters, s);
-  return p.ch == 1 ? launch_decode_out<32, 1, Q>(a, p, ws, counters, s)
-                   : launch_decode_out<32, 2, Q>(a, p, ws, counters, s);
+    return p.ch == 1 ? launch_decode_out<16, 1, Q, NV>(a, p, ws, counters, s)
+                     : launch_decode_out<16, 4, Q, NV>(a, p, ws, counters, s);
+  return p.ch == 1 ? launch_decode_out<32, 1, Q, NV>(a, p, ws, counters, s)
+                   : launch_decode_out<32, 2, Q, NV>(a, p, ws, counters, s);
 }
 }  // namespace
 
@@ -1043,8 +1089,12 @@ cudaError_t launch_gemm_mxfp4_decode(const Mxfp4GemmArgs& a, int num_sms, cudaSt
   float* ws = static_cast<float*>(a.workspace);
   uint32_t* counters =
       ws == nullptr ? nullptr : reinterpret_cast<uint32_t*>(ws + p.tiles * p.smax * p.nx * 128);
-  return a.xsrc != nullptr ? launch_decode_shape<true>(a, p, ws, counters, s)
-                           : launch_decode_shape<false>(a, p, ws, counters, s);
+  // NVFP4 (a.nvfp4, scales UE4M3 per 16, result times a.alpha) takes
+  // quantised activations only
+  if (a.nvfp4)
+    return a.xsrc != nullptr ? cudaErrorInvalidValue : launch_decode_shape<false, true>(a, p, ws, counters, s);
+  return a.xsrc != nullptr ? launch_decode_shape<true, false>(a, p, ws, counters, s)
+                           : launch_decode_shape<false, false>(a, p, ws, counters, s);
 }
 
 }  // namespace bsg

@@ -239,7 +239,8 @@ bsg_status bsg_quantize_fp4_bs16(const void* x, bsg_dtype src, int64_t rows, int
  *         the tensor core, as bsg_quantize_mx writes them); E2M1 ->
  *         BSG_SCALE_BLOCK1x32_E8M0 in the BSG_SF_TCGEN05 layout (MXFP4), or
  *         BSG_SCALE_BLOCK1x16_E4M3 in that layout for both operands (NVFP4,
- *         alpha 1; see bsg_gemm_nvfp4), or BSG_SCALE_BLOCK1x32_BF16 /
+ *         alpha 1; see bsg_gemm_nvfp4; up to 32 rows the decode-shaped
+ *         kernel, which needs the workspace as for MXFP4), or BSG_SCALE_BLOCK1x32_BF16 /
  *         BSG_SCALE_BLOCK1x32_F16 for both operands ([K/32][M] 16-bit codes,
  *         as bsg_quantize_fp4_bs16 writes them).
  * sB, gb  B's scales, same rules with N in place of M.
@@ -303,12 +304,38 @@ bsg_status bsg_gemm_quantized(int64_t M, int64_t N, int64_t K,
  * g_A * g_B) multiplies the FP32 sum before the addend C (optional FP32
  * M x N).  D: FP32 or BF16 (nearest even), M x N row-major.  bsg_gemm with
  * BSG_SCALE_BLOCK1x16_E4M3 on both operands is the same with alpha = 1.
+ * Up to M = 32 rows that takes the decode-shaped kernel, and so does
+ * bsg_gemm_nvfp4_ws below; this entry point has no workspace, so for M <= 32
+ * it runs the decode-shaped kernel only when no split-K workspace is needed
+ * (bsg_gemm_workspace_size(M, N, K, BSG_E2M1, BSG_E2M1) == 0), else the
+ * general kernel.
  * Constraints: K % 32 == 0; A, B, sA, sB 16-byte aligned.
  * Errors: BSG_ERR_INVALID_ARG, BSG_ERR_ALIGNMENT, BSG_ERR_CUDA.
  */
 bsg_status bsg_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const void* A, const void* sA,
                           const void* B, const void* sB, float alpha, const float* C, void* D,
                           bsg_dtype out, void* stream);
+
+/* bsg_gemm_nvfp4_ws - bsg_gemm_nvfp4 with a workspace, for the decode shapes
+ * of "Rubin FP4 GEMM deep dive" (section 5.3, blocks of 16 with E4M3
+ * scales; a memory-bound GEMM whose few activation rows meet a large weight
+ * matrix).
+ *
+ * Same arguments, result and constraints as bsg_gemm_nvfp4, plus workspace,
+ * workspace_bytes: device scratch of at least
+ * bsg_gemm_workspace_size(M, N, K, BSG_E2M1, BSG_E2M1) bytes (NULL when that
+ * is 0), zero-filled before its first use and left zero-filled by every
+ * successful call; calls that share a workspace must not overlap in time.
+ * For M <= 32 the call runs the decode-shaped kernel: the weights B are the
+ * tensor core's 128-row operand and stream from HBM once, and K is split
+ * evenly over all SMs (partial sums added in a fixed order, so results do
+ * not depend on timing).  Larger M: as bsg_gemm_nvfp4.
+ * Errors: as bsg_gemm_nvfp4, plus BSG_ERR_WORKSPACE (a workspace given that
+ *     is smaller than needed or not 16-byte aligned).
+ */
+bsg_status bsg_gemm_nvfp4_ws(int64_t M, int64_t N, int64_t K, const void* A, const void* sA,
+                             const void* B, const void* sB, float alpha, const float* C, void* D,
+                             bsg_dtype out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of device workspace bsg_gemm needs for this problem (0 if none). */
 size_t bsg_gemm_workspace_size(int64_t M, int64_t N, int64_t K, bsg_format fa, bsg_format fb);

@@ -272,3 +272,11 @@ def test_mxfp4_decode_bit_exact_when_k_is_one_work_unit(M):
     # the decode kernel splits K over the SMs in units of 256; with K = 256
     # every tile is one unit, so its result is one MMA chain as well
     _run_gemm("mxfp4", M, 1000, 256, "f32", True, 500 + M, n=4000)
+
+
+@pytest.mark.parametrize("M", [1, 16, 32])
+def test_nvfp4_decode_bit_exact_when_k_is_one_work_unit(M):
+    # NVFP4 through the decode kernel (bsg_gemm_nvfp4 with the workspace the
+    # binding supplies): with K = 256 every tile is one work unit, one MMA
+    # chain, so the result is the emulated one bit for bit, alpha included
+    _run_gemm("nvfp4", M, 1000, 256, "bf16", True, 600 + M, alpha=0.3, n=4000)

@@ -103,3 +103,62 @@ def test_nvfp4_large_kernel_ragged(M, N, K, out, addend):
 def test_nvfp4_large_kernel_through_bsg_gemm():
     report("nvfp4 large via bsg_gemm", *_gemm(1536, 2048, 512, ga=1.0, gb=1.0, via_bsg_gemm=True,
                                               rows=np.arange(0, 1536, 5)))
+
+
+# Decode shapes (M <= 32) take the swap-AB kernel that streams the weights
+# once and splits K evenly over the SMs: ragged N, N below one 128-row tile,
+# K tails that leave a partial 128-byte chunk (K % 256 != 0), split tiles.
+@pytest.mark.parametrize("M", [1, 7, 16, 17, 32])
+@pytest.mark.parametrize("N,K", [(1000, 1024), (4096, 8192), (384, 96), (2048, 2304)])
+def test_nvfp4_decode(M, N, K):
+    report(f"nvfp4 decode {M}x{N}x{K}", *_gemm(M, N, K, ga=1.0, gb=2.0 ** -6, out="bf16",
+                                              addend=M % 2 == 1, workload="decode"))
+
+
+@pytest.mark.parametrize("M", [1, 16, 32])
+def test_nvfp4_decode_through_bsg_gemm(M):
+    report(f"nvfp4 decode via bsg_gemm M={M}", *_gemm(M, 2048, 4096, ga=1.0, gb=1.0, out="f32", addend=True,
+                                                     via_bsg_gemm=True, workload="decode"))
+
+
+def test_nvfp4_decode_full_size_sampled_columns():
+    # the decode benchmark shape (N = 28672, K = 8192) at M = 16; the oracle
+    # checks output columns (weight rows) at tile edges, split boundaries and
+    # random places
+    N, K = 28672, 8192
+    rng = np.random.default_rng(11)
+    cols = np.unique(np.concatenate([np.arange(0, 4), np.arange(124, 132), np.arange(N - 4, N),
+                                     np.arange(128, N, 128 * 37), rng.integers(0, N, 256)]))
+    report(f"nvfp4 decode full size ({cols.size} columns)",
+           *_gemm(16, N, K, ga=1.0, gb=2.0 ** -6, out="bf16", cols=cols, workload="decode"))
+
+
+def test_nvfp4_decode_workspace_errors():
+    # a workspace that is given but too small is an error; none at all lets
+    # the call fall back to the general kernel
+    import ctypes
+    import fp4_gemm_gb300 as bsg
+    import torch
+    dev = device()
+    M, N, K = 16, 4096, 8192
+    need = bsg.bsg_gemm_workspace_size(M, N, K, "e2m1", "e2m1")
+    assert need > 0
+    A, B = synth.make("decode", m=M, n=N, k=K)
+    qa, sa = bsg.bsg_quantize_nvfp4(to_dev(A, dev))
+    qb, sb = bsg.bsg_quantize_nvfp4(to_dev(B, dev), tensor_scale=2.0 ** -6)
+    D = torch.empty((M, N), dtype=torch.float32, device=dev)
+    small = torch.zeros(64, dtype=torch.uint8, device=dev)
+    lib = bsg.load_library()
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    assert lib.bsg_gemm_nvfp4_ws(M, N, K, p(qa), p(sa), p(qb), p(sb), 2.0 ** -6, None, p(D), 0, p(small), 64,
+                                 None) == 6
+    D1 = bsg.bsg_gemm_nvfp4(qa, sa, qb, sb, alpha=2.0 ** -6)
+    assert lib.bsg_gemm_nvfp4(M, N, K, p(qa), p(sa), p(qb), p(sb), 2.0 ** -6, None, p(D), 0, None) == 0
+    torch.cuda.synchronize()
+    assert bsg.bsg_device_error() == 0
+    # decode-shaped and general kernels agree within the tolerance
+    pa, fa = oq.quantize_nvfp4(A)
+    pb, fb = oq.quantize_nvfp4(B, tensor_scale=2.0 ** -6)
+    Dref, bnd = og.gemm_nvfp4(pa, fa, pb, fb, alpha=2.0 ** -6)
+    for X in (D1, D):
+        report("nvfp4 decode / general", *og.within_tolerance(X.float().cpu().numpy(), Dref, bnd))
