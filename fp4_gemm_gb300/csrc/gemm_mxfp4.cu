@@ -26,9 +26,10 @@
 //    kind::mxf4nvf4 scale_vec::4X, the sum times alpha).  It serves problems
 //    with few tiles; larger FP4 problems go to the 128 x 256 block-scaled
 //    kernel of gemm_mx.cu.
-//  * gemm_mxfp4_decode_kernel: decode shapes (M <= 32 activation rows).  The
-//    weights are the MMA's 128-row operand and the activations its N = 16/32
-//    operand ("swap AB"), so the weight matrix streams from HBM exactly once.
+//  * gemm_mxfp4_decode_kernel: decode shapes (M <= 32 activation rows), in
+//    MXFP4 or NVFP4 form (kNv).  The weights are the MMA's 128-row operand
+//    and the activations its N = 16/32 operand ("swap AB"), so the weight
+//    matrix streams from HBM exactly once.
 //    Work is split evenly over all SMs in units of (128 weight rows, 256 K);
 //    a CTA whose range covers only part of a tile's K writes an FP32 partial
 //    to the workspace, and the last contributor (per-tile counter) adds the
