@@ -82,6 +82,11 @@ def test_newer_entry_points_reject_bad_arguments_before_launch():
     assert lib.bsg_gemm_nvfp4(4, 4, 48, 16, 16, 16, 16, 1.0, None, 16, f32, None) == 1
     assert lib.bsg_gemm_nvfp4(4, 4, 64, 16, 16, 16, 16, float("nan"), None, 16, f32, None) == 1
     assert lib.bsg_gemm_nvfp4(4, 4, 64, 16, 24, 16, 16, 1.0, None, 16, f32, None) == 3
+    # bsg_gemm_nvfp4_ws validates the same way before it looks at the workspace
+    assert lib.bsg_gemm_nvfp4_ws(4, 4, 48, 16, 16, 16, 16, 1.0, None, 16, f32, 16, 64, None) == 1
+    assert lib.bsg_gemm_nvfp4_ws(4, 4, 64, 16, 16, 16, 16, float("inf"), None, 16, f32, 16, 64, None) == 1
+    assert lib.bsg_gemm_nvfp4_ws(4, 4, 64, 16, 16, 24, 16, 1.0, None, 16, f32, 16, 64, None) == 3
+    assert lib.bsg_gemm_nvfp4_ws(0, 4, 64, 16, 16, 16, 16, 1.0, None, 16, f32, None, 0, None) == 1
     # bsg_gemm: NVFP4 scales on one operand only
     assert lib.bsg_gemm(4, 4, 64, 16, e2m1, 16, nv, 16, e2m1, 16, mx, None, 16, f32, None, 0, None) == 2
     # scale sizes of the 1 x 16 E4M3 granularity
