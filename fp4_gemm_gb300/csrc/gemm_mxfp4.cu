@@ -538,6 +538,16 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// L2 prefetch of the weight-scale atoms of work unit u.  Not inlined, like
+// prefetch_first_stages below.
+__device__ __noinline__ void prefetch_scale_atoms(const uint8_t* sfW, int64_t u, int64_t KS, int KA, int CH,
+                                                  int apc) {
+  const int64_t tile = u / KS;
+  const int ka0 = apc * static_cast<int>(u % KS) * CH;
+  const int na = min(apc * CH, KA - ka0);
+  if (na > 0) bulk_prefetch_l2(sfW + (tile * KA + ka0) * kSfAtom, static_cast<uint32_t>(na * kSfAtom));
+}
+
 // L2 prefetch of the weight boxes and weight-scale atoms of a decode CTA's
 // first `stages` units (the coordinates its producer and scale writers load
 // them with).  Not inlined: its registers stay out of the kernel's roles.
@@ -656,6 +666,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           tma_load_3d_hint(smem_u32(sm.w[s]), &tmW, fb, 0, static_cast<int32_t>(tile * 128), c0, stream);
           if (!kQ) tma_load_3d_hint(smem_u32(sm.x[s]), &tmX, fb, 0, 0, c0, keep);
         }
+        // the weight-scale atoms of the unit kStages ahead go into L2, so
+        // that the scale writers' loads of them hit L2
+        if (u + kStages < u1) prefetch_scale_atoms(sfW, u + kStages, KS, KA, CH, kApc);
       }
       drain_fills(sm.full, kStages, it);
     }
